@@ -1,0 +1,130 @@
+"""ctypes wrapper over the float64 C++ RVQ oracle (rvq_oracle.cpp).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg may use it; the CUDA path never does.  Nothing here imports the
+CUDA package, and the CUDA package imports nothing from here.
+
+Functions
+---------
+encode(weights, x, n_q, threads=0) -> dict(codes, gap, best_dist, residual)
+    The residual loop of omnivoice.cpp ARCHITECTURE.md, "RVQ codec", in float64.
+decode(weights, codes, n_q, threads=0) -> (y float64 [N][D], n_bad)
+    The accumulated decode graph of the same section, in float64.
+reconstruct(weights, x, n_q) -> dict(codes, ..., x_hat)
+    decode(encode(x)).
+
+`weights` is a dict of float32 numpy arrays: w_in [Q][d][D], codebook [Q][K][d],
+w_out [Q][D][d], and optionally b_in [Q][d] and b_out [Q][D] (None = zero).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rvq_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "librvq_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (IEEE float64, no contraction into FMA)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread", "-ffp-contract=off",
+               "-fno-fast-math", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            f = ctypes.c_void_p
+            lib.rvq_oracle_encode.argtypes = [ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int] + [f] * 4 + [ctypes.c_int]
+            lib.rvq_oracle_encode.restype = ctypes.c_int
+            lib.rvq_oracle_decode.argtypes = [ctypes.c_int] * 4 + [f] * 4 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
+            lib.rvq_oracle_decode.restype = ctypes.c_int
+            lib.rvq_oracle_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _dims(weights):
+    Q, d, D = weights["w_in"].shape
+    K = weights["codebook"].shape[1]
+    assert weights["codebook"].shape == (Q, K, d)
+    assert weights["w_out"].shape == (Q, D, d)
+    if weights.get("b_in") is not None:
+        assert weights["b_in"].shape == (Q, d)
+    if weights.get("b_out") is not None:
+        assert weights["b_out"].shape == (Q, D)
+    return D, d, K, Q
+
+
+def encode(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 0,
+           want_residual: bool = True) -> dict:
+    lib = _load()
+    D, d, K, Q = _dims(weights)
+    n_q = Q if n_q is None else int(n_q)
+    x = _f32(x)
+    N = x.shape[0]
+    assert x.shape == (N, D)
+    w = {k: _f32(weights.get(k)) for k in ("w_in", "b_in", "codebook", "w_out", "b_out")}
+    codes = np.empty((N, n_q), dtype=np.int32)
+    gap = np.empty((N, n_q), dtype=np.float64)
+    best = np.empty((N, n_q), dtype=np.float64)
+    resid = np.empty((N, D), dtype=np.float64) if want_residual else None
+    rc = lib.rvq_oracle_encode(D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
+                               _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(x), N, n_q, _ptr(codes),
+                               _ptr(gap), _ptr(best), _ptr(resid), int(threads))
+    if rc != 0:
+        raise ValueError("rvq_oracle_encode rejected its arguments")
+    return {"codes": codes, "gap": gap, "best_dist": best, "residual": resid}
+
+
+def decode(weights: dict, codes: np.ndarray, n_q: int | None = None, threads: int = 0):
+    lib = _load()
+    D, d, K, Q = _dims(weights)
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    N = codes.shape[0]
+    n_q = codes.shape[1] if n_q is None else int(n_q)
+    assert codes.shape == (N, n_q)
+    w = {k: _f32(weights.get(k)) for k in ("codebook", "w_out", "b_out")}
+    y = np.empty((N, D), dtype=np.float64)
+    n_bad = ctypes.c_int64(0)
+    rc = lib.rvq_oracle_decode(D, d, K, Q, _ptr(w["codebook"]), _ptr(w["w_out"]), _ptr(w["b_out"]),
+                               _ptr(codes), N, n_q, _ptr(y), ctypes.addressof(n_bad), int(threads))
+    if rc != 0:
+        raise ValueError("rvq_oracle_decode rejected its arguments")
+    return y, int(n_bad.value)
+
+
+def reconstruct(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 0) -> dict:
+    enc = encode(weights, x, n_q, threads)
+    y, _ = decode(weights, enc["codes"], enc["codes"].shape[1], threads)
+    enc["x_hat"] = y
+    return enc
+
+
+def version() -> str:
+    return _load().rvq_oracle_version().decode()
