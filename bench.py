@@ -1,0 +1,321 @@
+"""Benchmark: RVQ encode + decode throughput (frames/s) on GB300.
+
+One step is one pass of the whole hot path over one batch of frames:
+rvq_encode (frames -> per-stage codes) then rvq_decode (codes -> summed
+reconstruction), through the C ABI.  The workload is the large-batch
+throughput case: B=256 x T=750 = 192 000 frames, D=1024, Q=8, K=1024, d=64,
+float32, planted codes with noise sigma=0.2 (many near-ties).  Its input
+(786 MB) and output (786 MB) are each larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
+on the host cores instead (a bounded sample of the same workload per step).
+Under torchrun each rank runs a full batch of its own (weak scaling, replicas:
+the frames are independent and no data-path collective exists).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import rvq_inputs as ri  # noqa: E402
+
+WORKLOAD = "large_batch"
+METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
+L2_BYTES = 129 * 2 ** 20
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def encode_flops_per_frame(w) -> float:
+    # stage projections (2*D*d per stage) + distances (2*K*d per stage)
+    return w.Q * (2.0 * w.D * w.d + 2.0 * w.K * w.d)
+
+
+def decode_bytes_per_frame(w) -> float:
+    # read n_q int32 codes, write D float32 outputs
+    return 4.0 * (w.Q + w.D)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The float64 CPU oracle on the host cores, a bounded sample per step."""
+    import oracle
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    w = ri.WORKLOAD_BY_NAME[WORKLOAD]
+    W = ri.make_weights(w)
+    sample = args.ref_frames
+    x = ri.make_x(w, W, rows=np.arange(sample))
+    cores = os.cpu_count() or 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        enc = oracle.encode(W, x, want_residual=False, threads=cores)
+        oracle.decode(W, enc["codes"], threads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * sum(times) / len(times)
+    value = sample / (ms / 1000.0)
+    desc = f"first {sample} frames of the {w.N}-frame workload per step (encode + decode, float64)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe(), "frames_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def cpu_baseline_leg(W, x_sample: np.ndarray, w) -> dict:
+    import oracle
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    enc = oracle.encode(W, x_sample, want_residual=False, threads=cores)
+    oracle.decode(W, enc["codes"], threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": x_sample.shape[0] / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
+            "sample": f"{x_sample.shape[0]} frames of the {w.N}-frame workload, encode + decode in float64, "
+                      f"{dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import residual_vector_quantisation_gb300 as rq
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = ri.WORKLOAD_BY_NAME[WORKLOAD]
+    W = ri.make_weights(w)
+    Wt = ri.weights_to_torch(W, dev)
+    rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev)
+    # each rank encodes its own batch of the workload's shape: shift the frame seed per rank
+    wr = ri.Workload(w.name, w.B, w.T, w.D, w.Q, w.K, w.d, w.kind, w.sigma, w.cb_decay, w.seed + 1000 * rank) \
+        if rank else w
+    x = ri.make_x_torch(wr, Wt, dev)
+    N, n_q = w.N, w.Q
+    codes = torch.empty((N, n_q), dtype=torch.int32, device=dev)
+    y = torch.empty((N, w.D), dtype=torch.float32, device=dev)
+    scratch = rvq.scratch_for(N, n_q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rq.rvq_encode(rvq.dims, rvq.tables, x, n_q, codes, scratch, stream)
+        rq.rvq_decode(rvq.dims, rvq.tables, codes, n_q, y, None, stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    # timed region: whole steps, plus per-call events for the kernel-level roofline
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            rq.rvq_encode(rvq.dims, rvq.tables, x, n_q, codes, scratch, stream)
+            ev[i][1].record(stream)
+            rq.rvq_decode(rvq.dims, rvq.tables, codes, n_q, y, None, stream)
+            ev[i][2].record(stream)
+        stop.record(stream)
+        barrier()
+    ms_total = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    # end to end through the public API: pinned host frames in, host codes + reconstruction out
+    x_host = x.cpu().pin_memory()
+    codes_host = torch.empty(codes.shape, dtype=codes.dtype, pin_memory=True)
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        c = rvq.encode(x_dev, codes=codes)
+        yy = rvq.decode(c, y=y)
+        codes_host.copy_(c, non_blocking=True)
+        y_host.copy_(yy, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, args.steps // 2)
+    e_start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e_stop.record(stream)
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_stop) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        peaks = _peaks()
+        clk = clocks.summary()
+        # encode: FP32 SIMT kernels; the ALU peak is SMs x 128 lanes x 2 FLOP x max SM clock
+        fp32_peak_tflops = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        enc_achieved = encode_flops_per_frame(w) * N / (enc_ms / 1e3) / 1e12
+        dec_achieved = decode_bytes_per_frame(w) * N / (dec_ms / 1e3) / 1e9
+        scratch_rows = scratch.numel() // (n_q * w.d * 4)
+        chunk = N if scratch_rows >= N else scratch_rows // 128 * 128
+        n_chunks = math.ceil(N / chunk)
+        launches_per_step = 2 * n_chunks + 1
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rows = args.cpu_frames
+            cpu = cpu_baseline_leg(W, x[:rows].cpu().numpy(), w)
+        value = world * N / (ms_step / 1e3)
+        out = {
+            "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.describe(), "frames_per_gpu": N, "parallelism": f"replicas{world}",
+                       "l2": "inputs and outputs larger than L2 (786 MB each); no flush",
+                       "step": "rvq_encode + rvq_decode through the C ABI"},
+            "encode_ms": enc_ms, "decode_ms": dec_ms,
+            "encode_frames_per_s": N / (enc_ms / 1e3), "decode_frames_per_s": N / (dec_ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": enc_achieved, "peak": fp32_peak_tflops, "unit": "TFLOP/s",
+                         "frac": enc_achieved / fp32_peak_tflops, "traffic": None,
+                         "kernel": "encode (projection GEMM + stage search, FP32 SIMT)",
+                         "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
+                                       f"{peaks['sm_max_mhz']:.0f} MHz"},
+            "roofline_decode": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": dec_achieved / peaks["hbm_gbs"], "traffic": None,
+                                "peak_basis": f"{peaks['source']} HBM copy bandwidth"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * N / (e2e_ms / 1e3), "unit": "frames/s",
+                    "h2d_bytes_per_step": N * w.D * 4, "d2h_bytes_per_step": N * w.D * 4 + N * n_q * 4},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-frames", type=int, default=49152, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-frames", type=int, default=8192, help="oracle frames per step for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * rvq.h -- C ABI for residual vector quantisation (RVQ) encode and decode on
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Plain C99, extern "C", only rvq_* symbols exported.  Conventions follow the
+ * plain-C ABI discipline of omnivoice.cpp ARCHITECTURE.md, sections "Public
+ * API" and "ABI guarantee": a status enum where 0 is success and negative
+ * values are errors, and a header that C, C++ and ctypes consume alike.  The
+ * operation set (encode, decode, reconstruct, prefix depth) follows the codec
+ * API of moss-tts.cpp AGENTS.md ("Layout": moss::Codec encode / decode /
+ * reconstruct) and its bitrate control (gotcha 12: use the first k stages).
+ *
+ * What is computed (omnivoice.cpp ARCHITECTURE.md, section "RVQ codec"):
+ *   encode, per frame, for stage q = 0 .. n_q-1:
+ *     p_q       = w_in[q] . residual + b_in[q]
+ *     code_q    = argmin_k || p_q - codebook[q][k] ||^2   (lowest k on ties)
+ *     residual -= w_out[q] . codebook[q][code_q] + b_out[q]
+ *   decode:  y = sum_{q < n_q} ( w_out[q] . codebook[q][code_q] + b_out[q] )
+ *   with residual = x on entry.
+ *
+ * Shapes and layouts (all float32 row-major, PyTorch (out, in) layouts as in
+ * that section's tensor table):
+ *   w_in     [Q][d][D]      b_in  [Q][d]  (nullable: zero)
+ *   codebook [Q][K][d]
+ *   w_out    [Q][D][d]      b_out [Q][D]  (nullable: zero)
+ *   x, y, x_hat [N][D]      frame-major: one contiguous feature vector per frame
+ *   codes    [N][n_q] int32 frame-major (moss-tts.cpp AGENTS.md, gotcha 8)
+ *
+ * Memory and ownership.  Every pointer except the struct pointers is DEVICE
+ * memory owned by the caller.  The library allocates nothing, frees nothing
+ * and never synchronises the stream: each call validates its arguments on the
+ * host, enqueues kernels on `stream` and returns.  Results are ready when the
+ * stream reaches that point.
+ *   tables  -- written by rvq_prepare, read-only afterwards; the weights are
+ *              not read again, so they may be freed after rvq_prepare's work
+ *              has completed on its stream.  One tables buffer may serve
+ *              concurrent calls on several streams.
+ *   scratch -- per-call working memory of rvq_encode / rvq_reconstruct.
+ *              Calls that may overlap on the GPU need separate scratch.
+ *
+ * Errors.  Arguments are checked before any launch:
+ *   RVQ_ERR_INVALID_ARG  null pointer, n_frames < 0, n_q outside [1, Q], a
+ *                        tables or scratch buffer smaller than required, a
+ *                        device pointer not 16-byte aligned;
+ *   RVQ_ERR_UNSUPPORTED  shapes the kernels do not handle (see
+ *                        rvq_dims_supported);
+ *   RVQ_ERR_CUDA         a launch failed (cudaGetLastError after launch).
+ * n_frames == 0 is valid and enqueues nothing.  Inputs must be finite; the
+ * result for NaN or Inf inputs is unspecified.  Codes given to rvq_decode
+ * outside [0, K) contribute nothing and are counted (see rvq_decode).
+ */
+#ifndef RVQ_H
+#define RVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(_WIN32)
+#define RVQ_API
+#else
+#define RVQ_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RVQ_VERSION_MAJOR 0
+#define RVQ_VERSION_MINOR 1
+#define RVQ_VERSION_PATCH 0
+
+typedef enum rvq_status {
+  RVQ_OK = 0,
+  RVQ_ERR_INVALID_ARG = -1,
+  RVQ_ERR_UNSUPPORTED = -2,
+  RVQ_ERR_WORKSPACE = -3,
+  RVQ_ERR_CUDA = -4,
+  RVQ_ERR_TIMEOUT = -5
+} rvq_status;
+
+/* D: frame (feature) dimension; d: code-space dimension; K: entries per
+ * codebook; Q: number of stages held in the tables. */
+typedef struct rvq_dims {
+  int32_t D;
+  int32_t d;
+  int32_t K;
+  int32_t Q;
+} rvq_dims;
+
+/* Device pointers to the per-stage tensors (layouts above). */
+typedef struct rvq_weights {
+  const float *w_in;
+  const float *b_in;
+  const float *codebook;
+  const float *w_out;
+  const float *b_out;
+} rvq_weights;
+
+/* Same type as cudaStream_t; the header needs no CUDA include.  NULL is the
+ * legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *rvq_stream_t;
+
+/* RVQ_OK if the kernels handle these dims, else RVQ_ERR_UNSUPPORTED (or
+ * RVQ_ERR_INVALID_ARG for non-positive values).  Supported: d == 64,
+ * K a multiple of 128 with K <= 65536, D a multiple of 16 with D <= 16384,
+ * 1 <= Q <= 64. */
+RVQ_API rvq_status rvq_dims_supported(rvq_dims dims);
+
+/* Bytes of the tables buffer for these dims (0 if unsupported). */
+RVQ_API size_t rvq_tables_bytes(rvq_dims dims);
+
+/* Fill `tables` (tables_bytes >= rvq_tables_bytes(dims), 256-byte aligned)
+ * from the weights.  The tables hold, computed in float64 and rounded once to
+ * float32: squared codebook norms; the decode table
+ *   Z[q][k] = w_out[q] . codebook[q][k] + b_out[q]           ([Q][K][D]);
+ * and the cross-stage table
+ *   G[q][s][k] = w_in[q] . Z[s][k]   for s < q               ([Q(Q-1)/2][K][d]),
+ * which lets encode update every stage's projection without materialising the
+ * D-dimensional residual:  w_in[q] . residual_q = w_in[q] . x - sum_{s<q} G[q][s][code_s].
+ * Both are exact re-associations of the sums in the "RVQ codec" section.
+ * Also a copy of w_in split into TF32 high and low parts, and the codebook in
+ * the layouts the kernels read.  Asynchronous on `stream`. */
+RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *tables,
+                               size_t tables_bytes, rvq_stream_t stream);
+
+/* Scratch bytes rvq_encode / rvq_reconstruct need for n_frames frames at
+ * depth n_q.  Encode works through the frames in chunks whose per-frame stage
+ * projections ([chunk][n_q*d] float32) live in scratch; this returns the size
+ * that lets one chunk cover up to a bounded number of frames (about 32 MiB).
+ * A larger scratch is accepted and used for larger chunks; a smaller one (at
+ * least rvq_encode_min_scratch_bytes) gives smaller chunks. */
+RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q);
+RVQ_API size_t rvq_encode_min_scratch_bytes(rvq_dims dims, int32_t n_q);
+
+/* Encode n_frames frames x [N][D] with the first n_q stages (1 <= n_q <= Q)
+ * into codes [N][n_q].  Each code is the argmin of the squared L2 distance,
+ * lowest index on ties.  The distances are computed to about float32
+ * accuracy; where two entries' distances differ by less than that, either
+ * may be returned. */
+RVQ_API rvq_status rvq_encode(rvq_dims dims, const void *tables, const float *x, int64_t n_frames,
+                              int32_t n_q, int32_t *codes, void *scratch, size_t scratch_bytes,
+                              rvq_stream_t stream);
+
+/* Decode codes [N][n_q] into y [N][D]:
+ *   y[n] = sum_{q < n_q} Z[q][codes[n][q]]   (summed in stage order, float32).
+ * A code outside [0, K) contributes nothing; if bad_codes (device, int64) is
+ * not NULL, the number of such codes is added to *bad_codes (atomically; the
+ * caller zeroes it). */
+RVQ_API rvq_status rvq_decode(rvq_dims dims, const void *tables, const int32_t *codes,
+                              int64_t n_frames, int32_t n_q, float *y, int64_t *bad_codes,
+                              rvq_stream_t stream);
+
+/* Encode then decode: codes [N][n_q] (required) and x_hat [N][D] = decode(codes),
+ * the quantised reconstruction of x (x - x_hat is the final residual). */
+RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const float *x,
+                                   int64_t n_frames, int32_t n_q, int32_t *codes, float *x_hat,
+                                   void *scratch, size_t scratch_bytes, rvq_stream_t stream);
+
+/* Static strings. */
+RVQ_API const char *rvq_status_string(rvq_status status);
+RVQ_API const char *rvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RVQ_H */

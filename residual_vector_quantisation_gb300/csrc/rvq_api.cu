@@ -1,0 +1,154 @@
+// Host entry points of the C ABI declared in include/rvq.h.
+//
+// Every entry point validates its arguments on the host before touching the
+// CUDA runtime, so the early-return paths work on a machine with no GPU.
+// Nothing here allocates, frees or synchronises.
+#include <stdint.h>
+
+#include "rvq_internal.cuh"
+
+namespace rvq {
+size_t search_smem_bytes(int n_q);
+}
+
+namespace {
+
+using rvq::TablesLayout;
+
+constexpr size_t kChunkTargetBytes = size_t(32) << 20;  // projections per encode chunk (L2-resident)
+constexpr int64_t kChunkQuantum = 128;                   // frames
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+rvq_status check_dims(const rvq_dims &dm) {
+  if (dm.D <= 0 || dm.d <= 0 || dm.K <= 0 || dm.Q <= 0) return RVQ_ERR_INVALID_ARG;
+  if (dm.d != rvq::kCodeDim) return RVQ_ERR_UNSUPPORTED;
+  if (dm.K % 128 != 0 || dm.K > 65536) return RVQ_ERR_UNSUPPORTED;
+  if (dm.D % 16 != 0 || dm.D > 16384) return RVQ_ERR_UNSUPPORTED;
+  if (dm.Q > rvq::kMaxStages) return RVQ_ERR_UNSUPPORTED;
+  return RVQ_OK;
+}
+
+size_t row_bytes(const rvq_dims &dm, int32_t n_q) { return (size_t)n_q * dm.d * sizeof(float); }
+
+// Frames per encode chunk for a given scratch size (0 if the scratch is too small).
+int64_t chunk_frames(const rvq_dims &dm, int32_t n_q, int64_t n_frames, size_t scratch_bytes) {
+  const size_t rb = row_bytes(dm, n_q);
+  int64_t fit = (int64_t)(scratch_bytes / rb);
+  if (fit >= n_frames) return n_frames;
+  fit = fit / kChunkQuantum * kChunkQuantum;
+  return fit;
+}
+
+rvq_status launch_status(cudaError_t e) { return e == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA; }
+
+rvq_status encode_impl(const rvq_dims &dm, const void *tables, const float *x, int64_t n_frames, int32_t n_q,
+                       int32_t *codes, void *scratch, size_t scratch_bytes, cudaStream_t st) {
+  const int64_t chunk = chunk_frames(dm, n_q, n_frames, scratch_bytes);
+  for (int64_t n0 = 0; n0 < n_frames; n0 += chunk) {
+    const int64_t n = (n_frames - n0 < chunk) ? n_frames - n0 : chunk;
+    cudaError_t e = rvq::launch_encode_chunk(dm, tables, x, n0, n, n_q, codes, static_cast<float *>(scratch), st);
+    if (e != cudaSuccess) return RVQ_ERR_CUDA;
+  }
+  return RVQ_OK;
+}
+
+rvq_status check_encode_args(const rvq_dims &dm, const void *tables, const float *x, int64_t n_frames, int32_t n_q,
+                             const int32_t *codes, const void *scratch, size_t scratch_bytes) {
+  rvq_status s = check_dims(dm);
+  if (s != RVQ_OK) return s;
+  if (n_frames < 0 || n_q < 1 || n_q > dm.Q) return RVQ_ERR_INVALID_ARG;
+  if (n_frames == 0) return RVQ_OK;
+  if (!tables || !x || !codes || !scratch) return RVQ_ERR_INVALID_ARG;
+  if (!aligned256(tables) || !aligned16(x) || !aligned16(scratch) || !aligned16(codes)) return RVQ_ERR_INVALID_ARG;
+  if (chunk_frames(dm, n_q, n_frames, scratch_bytes) <= 0) return RVQ_ERR_INVALID_ARG;
+  return RVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+RVQ_API rvq_status rvq_dims_supported(rvq_dims dims) { return check_dims(dims); }
+
+RVQ_API size_t rvq_tables_bytes(rvq_dims dims) {
+  if (check_dims(dims) != RVQ_OK) return 0;
+  return rvq::tables_layout(dims).total;
+}
+
+RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *tables, size_t tables_bytes,
+                               rvq_stream_t stream) {
+  rvq_status s = check_dims(dims);
+  if (s != RVQ_OK) return s;
+  if (!weights || !weights->w_in || !weights->codebook || !weights->w_out || !tables) return RVQ_ERR_INVALID_ARG;
+  if (!aligned256(tables) || !aligned16(weights->w_in) || !aligned16(weights->codebook) ||
+      !aligned16(weights->w_out))
+    return RVQ_ERR_INVALID_ARG;
+  if (tables_bytes < rvq::tables_layout(dims).total) return RVQ_ERR_INVALID_ARG;
+  return launch_status(rvq::launch_prepare(dims, *weights, tables, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+RVQ_API size_t rvq_encode_min_scratch_bytes(rvq_dims dims, int32_t n_q) {
+  if (check_dims(dims) != RVQ_OK || n_q < 1 || n_q > dims.Q) return 0;
+  return (size_t)kChunkQuantum * row_bytes(dims, n_q);
+}
+
+RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q) {
+  if (check_dims(dims) != RVQ_OK || n_q < 1 || n_q > dims.Q || n_frames < 0) return 0;
+  const size_t rb = row_bytes(dims, n_q);
+  int64_t target = (int64_t)(kChunkTargetBytes / rb) / kChunkQuantum * kChunkQuantum;
+  if (target < kChunkQuantum) target = kChunkQuantum;
+  const int64_t frames = n_frames < target ? (n_frames > 0 ? n_frames : 1) : target;
+  return (size_t)frames * rb;
+}
+
+RVQ_API rvq_status rvq_encode(rvq_dims dims, const void *tables, const float *x, int64_t n_frames, int32_t n_q,
+                              int32_t *codes, void *scratch, size_t scratch_bytes, rvq_stream_t stream) {
+  rvq_status s = check_encode_args(dims, tables, x, n_frames, n_q, codes, scratch, scratch_bytes);
+  if (s != RVQ_OK || n_frames == 0) return s;
+  return encode_impl(dims, tables, x, n_frames, n_q, codes, scratch, scratch_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+RVQ_API rvq_status rvq_decode(rvq_dims dims, const void *tables, const int32_t *codes, int64_t n_frames, int32_t n_q,
+                              float *y, int64_t *bad_codes, rvq_stream_t stream) {
+  rvq_status s = check_dims(dims);
+  if (s != RVQ_OK) return s;
+  if (n_frames < 0 || n_q < 1 || n_q > dims.Q) return RVQ_ERR_INVALID_ARG;
+  if (n_frames == 0) return RVQ_OK;
+  if (!tables || !codes || !y) return RVQ_ERR_INVALID_ARG;
+  if (!aligned256(tables) || !aligned16(y) || !aligned16(codes)) return RVQ_ERR_INVALID_ARG;
+  if (bad_codes && (reinterpret_cast<uintptr_t>(bad_codes) & 7u)) return RVQ_ERR_INVALID_ARG;
+  return launch_status(
+      rvq::launch_decode(dims, tables, codes, n_frames, n_q, y, bad_codes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const float *x, int64_t n_frames, int32_t n_q,
+                                   int32_t *codes, float *x_hat, void *scratch, size_t scratch_bytes,
+                                   rvq_stream_t stream) {
+  rvq_status s = check_encode_args(dims, tables, x, n_frames, n_q, codes, scratch, scratch_bytes);
+  if (s != RVQ_OK) return s;
+  if (n_frames == 0) return RVQ_OK;
+  if (!x_hat || !aligned16(x_hat)) return RVQ_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  s = encode_impl(dims, tables, x, n_frames, n_q, codes, scratch, scratch_bytes, st);
+  if (s != RVQ_OK) return s;
+  return launch_status(rvq::launch_decode(dims, tables, codes, n_frames, n_q, x_hat, nullptr, st));
+}
+
+RVQ_API const char *rvq_status_string(rvq_status status) {
+  switch (status) {
+    case RVQ_OK: return "ok";
+    case RVQ_ERR_INVALID_ARG: return "invalid argument";
+    case RVQ_ERR_UNSUPPORTED: return "unsupported shape";
+    case RVQ_ERR_WORKSPACE: return "workspace too small";
+    case RVQ_ERR_CUDA: return "CUDA launch failed";
+    case RVQ_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

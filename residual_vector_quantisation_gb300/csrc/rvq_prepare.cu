@@ -1,0 +1,166 @@
+// Table preparation: everything encode and decode read besides the frames.
+//
+// All sums run in float64 and are rounded once to float32, so each table
+// entry is the correctly rounded value of its exact-arithmetic definition up
+// to float64 summation error (about 1e-16 relative).
+//
+//   cnorm[q][k]   = ||codebook[q][k]||^2
+//   Z[q][k]       = w_out[q] . codebook[q][k] + b_out[q]         (decode table)
+//   G[q][s][k]    = w_in[q] . Z[s][k]            for s < q      (cross-stage table)
+//
+// Z re-associates the decode graph of omnivoice.cpp ARCHITECTURE.md ("RVQ
+// codec": gather, project_out, add bias, accumulate) into one gather per
+// stage.  G re-associates the encode loop of the same section: since
+// residual_q = x - sum_{s<q} Z[s][code_s], the stage-q projection is
+// w_in[q] . x + b_in[q] - sum_{s<q} G[q][s][code_s].
+#include "rvq_internal.cuh"
+
+namespace rvq {
+namespace {
+
+__device__ __forceinline__ float tf32_trunc(float v) {
+  return __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+}
+
+// w_in plain / TF32 hi / lo copies and b_in.
+__global__ void k_prep_w_in(const float *__restrict__ w_in, const float *__restrict__ b_in,
+                            float *__restrict__ plain, float *__restrict__ hi, float *__restrict__ lo,
+                            float *__restrict__ b_out_copy, int64_t n, int64_t nb) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = i; e < n; e += stride) {
+    float v = w_in[e];
+    float h = tf32_trunc(v);
+    plain[e] = v;
+    hi[e] = h;
+    lo[e] = v - h;
+  }
+  for (int64_t e = i; e < nb; e += stride) b_out_copy[e] = b_in ? b_in[e] : 0.0f;
+}
+
+// Codebook copy, code-space-major transpose and squared norms.
+__global__ void k_prep_codebook(const float *__restrict__ cb_in, float *__restrict__ cb,
+                                float *__restrict__ cbT, float *__restrict__ cnorm, int K, int d,
+                                int64_t n_rows) {
+  int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // row = q*K + k
+  if (r >= n_rows) return;
+  int q = (int)(r / K), k = (int)(r % K);
+  const float *src = cb_in + r * d;
+  double s = 0.0;
+  for (int j = 0; j < d; ++j) {
+    float v = src[j];
+    cb[r * d + j] = v;
+    cbT[((int64_t)q * d + j) * K + k] = v;
+    s += (double)v * (double)v;
+  }
+  cnorm[r] = (float)s;
+}
+
+// Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64).
+// grid: (ceil(D/256), Q*K/16); each block handles 16 codewords of one stage.
+__global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
+                                                const float *__restrict__ b_out,
+                                                const float *__restrict__ cb, float *__restrict__ z,
+                                                int D, int K) {
+  constexpr int d = kCodeDim;
+  __shared__ double sc[16][d];
+  const int64_t row0 = (int64_t)blockIdx.y * 16;  // q*K + k0
+  const int q = (int)(row0 / K);
+  for (int e = threadIdx.x; e < 16 * d; e += blockDim.x)
+    sc[e / d][e % d] = (double)cb[(row0 + e / d) * d + e % d];
+  __syncthreads();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= D) return;
+  const float *wr = w_out + ((int64_t)q * D + i) * d;
+  double w[d];
+#pragma unroll
+  for (int j = 0; j < d; ++j) w[j] = (double)wr[j];
+  const double bias = b_out ? (double)b_out[(int64_t)q * D + i] : 0.0;
+  for (int kk = 0; kk < 16; ++kk) {
+    double s = 0.0;
+#pragma unroll
+    for (int j = 0; j < d; ++j) s += w[j] * sc[kk][j];
+    z[(row0 + kk) * D + i] = (float)(s + bias);
+  }
+}
+
+// M[t][j][m] = sum_i w_in[q][j][i] w_out[s][i][m];  vb[t][j] = sum_i w_in[q][j][i] b_out[s][i].
+// grid: (P, d); block: d threads (one per m) plus one warp for vb.
+__global__ void k_prep_m(const float *__restrict__ w_in, const float *__restrict__ w_out,
+                         const float *__restrict__ b_out, double *__restrict__ m64,
+                         double *__restrict__ vb64, int D, int Q) {
+  constexpr int d = kCodeDim;
+  const int t = blockIdx.x, j = blockIdx.y;
+  int q = 1;
+  while ((int64_t)(q + 1) * q / 2 <= t) ++q;  // t = q(q-1)/2 + s
+  const int s = t - q * (q - 1) / 2;
+  const float *wi = w_in + ((int64_t)q * d + j) * D;
+  if (threadIdx.x < d) {
+    const int m = threadIdx.x;
+    const float *wo = w_out + (int64_t)s * D * d + m;
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) acc += (double)wi[i] * (double)wo[(int64_t)i * d];
+    m64[((int64_t)t * d + j) * d + m] = acc;
+  } else {
+    const int lane = threadIdx.x - d;  // one warp
+    double acc = 0.0;
+    if (b_out)
+      for (int i = lane; i < D; i += 32) acc += (double)wi[i] * (double)b_out[(int64_t)s * D + i];
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) vb64[(int64_t)t * d + j] = acc;
+  }
+  (void)Q;
+}
+
+// G[t][k][j] = sum_m M[t][j][m] codebook[s][k][m] + vb[t][j]   (f64 -> f32).
+// grid: (P, K/16); 256 threads = 16 codewords x 16 groups of 4 j.
+__global__ void __launch_bounds__(256) k_prep_g(const double *__restrict__ m64,
+                                                const double *__restrict__ vb64,
+                                                const float *__restrict__ cb, float *__restrict__ g,
+                                                int K) {
+  constexpr int d = kCodeDim;
+  __shared__ double sm[d][d + 1];
+  __shared__ double sc[16][d];
+  const int t = blockIdx.x;
+  int q = 1;
+  while ((int64_t)(q + 1) * q / 2 <= t) ++q;
+  const int s = t - q * (q - 1) / 2;
+  const int k0 = blockIdx.y * 16;
+  for (int e = threadIdx.x; e < d * d; e += blockDim.x) sm[e / d][e % d] = m64[(int64_t)t * d * d + e];
+  for (int e = threadIdx.x; e < 16 * d; e += blockDim.x)
+    sc[e / d][e % d] = (double)cb[(((int64_t)s * K) + k0 + e / d) * d + e % d];
+  __syncthreads();
+  const int kk = threadIdx.x / 16, jg = threadIdx.x % 16;
+  for (int u = 0; u < 4; ++u) {
+    const int j = jg * 4 + u;
+    double acc = vb64[(int64_t)t * d + j];
+    for (int m = 0; m < d; ++m) acc += sm[j][m] * sc[kk][m];
+    g[(((int64_t)t * K) + k0 + kk) * d + j] = (float)acc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t st) {
+  const TablesLayout L = tables_layout(dm);
+  const int D = dm.D, d = dm.d, K = dm.K, Q = dm.Q;
+  const int64_t nw = (int64_t)Q * d * D, P = n_pairs(Q);
+  k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in), at<float>(tables, L.w_in_hi),
+                                   at<float>(tables, L.w_in_lo), at<float>(tables, L.b_in), nw,
+                                   (int64_t)Q * d);
+  const int64_t rows = (int64_t)Q * K;
+  k_prep_codebook<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb),
+                                                                  at<float>(tables, L.cbT),
+                                                                  at<float>(tables, L.cnorm), K, d, rows);
+  k_prep_z<<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
+                                                                          at<float>(tables, L.z), D, K);
+  if (P > 0) {
+    k_prep_m<<<dim3((unsigned)P, d), d + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
+                                                      at<double>(tables, L.vb64), D, Q);
+    k_prep_g<<<dim3((unsigned)P, K / 16), 256, 0, st>>>(at<double>(tables, L.m64), at<double>(tables, L.vb64),
+                                                        w.codebook, at<float>(tables, L.g), K);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rvq

@@ -1,0 +1,48 @@
+/* Plain C99 consumer of include/rvq.h: includes the header and calls every
+ * entry point through an early-return path (no GPU needed).  Built with
+ * -std=c99 -Wall -Werror -pedantic, as the ABI discipline of omnivoice.cpp
+ * ARCHITECTURE.md ("ABI guarantee") asks of its own header. */
+#include <stdio.h>
+#include <string.h>
+
+#include "rvq.h"
+
+static int failures = 0;
+#define EXPECT(cond)                                                   \
+  do {                                                                 \
+    if (!(cond)) {                                                     \
+      fprintf(stderr, "abi_c: line %d: %s\n", __LINE__, #cond);        \
+      failures++;                                                      \
+    }                                                                  \
+  } while (0)
+
+int main(void) {
+  rvq_dims ok = {1024, 64, 1024, 8};
+  rvq_dims bad_d = {1024, 32, 1024, 8};
+  rvq_dims zero = {0, 64, 1024, 8};
+  rvq_weights w;
+  int32_t fake_codes[4];
+  memset(&w, 0, sizeof w);
+
+  EXPECT(rvq_dims_supported(ok) == RVQ_OK);
+  EXPECT(rvq_dims_supported(bad_d) == RVQ_ERR_UNSUPPORTED);
+  EXPECT(rvq_dims_supported(zero) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_tables_bytes(ok) > 0);
+  EXPECT(rvq_tables_bytes(bad_d) == 0);
+  EXPECT(rvq_encode_scratch_bytes(ok, 1000, 8) >= rvq_encode_min_scratch_bytes(ok, 8));
+  EXPECT(rvq_encode_min_scratch_bytes(ok, 9) == 0);
+  EXPECT(rvq_prepare(ok, NULL, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_prepare(ok, &w, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_encode(ok, NULL, NULL, 10, 8, NULL, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_encode(ok, NULL, NULL, 0, 8, NULL, NULL, 0, NULL) == RVQ_OK); /* empty batch */
+  EXPECT(rvq_encode(ok, NULL, NULL, 10, 0, NULL, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_encode(ok, NULL, NULL, -1, 8, NULL, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_decode(ok, NULL, fake_codes, 1, 8, NULL, NULL, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_decode(ok, NULL, NULL, 1, 9, NULL, NULL, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_reconstruct(bad_d, NULL, NULL, 1, 8, NULL, NULL, NULL, 0, NULL) == RVQ_ERR_UNSUPPORTED);
+  EXPECT(strcmp(rvq_status_string(RVQ_OK), "ok") == 0);
+  EXPECT(rvq_status_string(RVQ_ERR_CUDA) != NULL);
+  EXPECT(rvq_version() != NULL && strlen(rvq_version()) > 0);
+  if (failures == 0) printf("abi_c: ok\n");
+  return failures == 0 ? 0 : 1;
+}

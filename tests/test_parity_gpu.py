@@ -1,0 +1,245 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Codes follow the near-tie rule of rvq_compare; decoded and reconstructed
+frames must lie within 1e-4 * RMS of the oracle's decode of the same codes.
+Small workloads are compared on every frame; the full-size workloads run on
+the GPU at full size (the benchmark's launch configuration) and are compared
+on sampled frames, which the oracle computes frame by frame.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rvq_inputs as ri
+from rvq_compare import FLOAT_TOL, compare_codes, max_abs_rel_to_rms, rms
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import residual_vector_quantisation_gb300 as rq  # noqa: E402
+from residual_vector_quantisation_gb300 import build as rqb  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rqb.build_library()
+    rq.load_library()
+
+
+def make_rvq(W):
+    t = ri.weights_to_torch(W, DEV)
+    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV)
+
+
+def check_encode(W, x, codes_gpu, rows=None, n_q=None, x_rms=None, x_hat_gpu=None, label=""):
+    """Oracle-encode x[rows]; compare codes (near-tie rule) and x_hat."""
+    rows = np.arange(x.shape[0]) if rows is None else rows
+    xs = x[rows]
+    ref = oracle.encode(W, xs, n_q, want_residual=False)
+    cg = codes_gpu[rows]
+    res = compare_codes(cg, ref["codes"], ref["gap"])
+    assert res["n_fail"] == 0, f"{label}: code mismatches at clear decisions: {res}"
+    # decode tolerance: oracle decode of the GPU's codes
+    if x_hat_gpu is not None:
+        y_ref, _ = oracle.decode(W, cg, cg.shape[1])
+        r = x_rms if x_rms is not None else rms(x)
+        err = max_abs_rel_to_rms(x_hat_gpu[rows], y_ref, r)
+        assert err <= FLOAT_TOL, f"{label}: x_hat error {err:.3e} * RMS"
+    return res
+
+
+def run_small(W, x, n_q=None, label=""):
+    rvq = make_rvq(W)
+    xt = torch.from_numpy(x).to(DEV)
+    codes, x_hat = rvq.reconstruct(xt, n_q)
+    codes_e = rvq.encode(xt, n_q)
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    assert np.array_equal(c, codes_e.cpu().numpy()), "encode and reconstruct disagree"
+    res = check_encode(W, x, c, n_q=n_q, x_hat_gpu=x_hat.cpu().numpy(), label=label)
+    # decode through the decode entry point too
+    y = rvq.decode(codes).cpu().numpy()
+    assert np.array_equal(y, x_hat.cpu().numpy())
+    return res, c
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_workload_every_frame():
+    w = ri.WORKLOAD_BY_NAME["tiny"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    res, _ = run_small(W, x, label="tiny")
+    assert res["n_equal"] >= 0.99 * res["n_stages"]
+
+
+def test_omnivoice_workload_every_frame():
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    res, c = run_small(W, x, label="omnivoice")
+    assert res["n_equal"] >= 0.99 * res["n_stages"]
+
+
+def test_decode_only_workload_sampled():
+    w = ri.WORKLOAD_BY_NAME["decode_only"]
+    W = ri.make_weights(w)
+    codes = ri.make_codes(w)
+    rvq = make_rvq(W)
+    ct = torch.from_numpy(codes).to(DEV)
+    bad = torch.zeros(1, dtype=torch.int64, device=DEV)
+    y = rvq.decode(ct, bad_codes=bad)
+    torch.cuda.synchronize()
+    assert int(bad.item()) == 0
+    rows = np.random.default_rng(0).choice(w.N, 4096, replace=False)
+    rows = np.concatenate([rows, [0, w.N - 1]])
+    y_ref, _ = oracle.decode(W, codes[rows])
+    yg = y[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    err = max_abs_rel_to_rms(yg, y_ref, rms(y_ref))
+    assert err <= FLOAT_TOL, f"decode error {err:.3e} * RMS(y)"
+
+
+def test_moss_deep_workload_sampled():
+    w = ri.WORKLOAD_BY_NAME["moss_deep"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    rvq = make_rvq(W)
+    xt = torch.from_numpy(x).to(DEV)
+    codes, x_hat = rvq.reconstruct(xt)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(1).choice(w.N, 2500, replace=False))
+    res = check_encode(W, x, codes.cpu().numpy(), rows=rows, x_rms=rms(x), x_hat_gpu=x_hat.cpu().numpy(),
+                       label="moss_deep")
+    assert res["n_equal"] >= 0.97 * res["n_stages"]
+
+
+def test_large_batch_workload_full_size_sampled():
+    """192 000 frames encoded and decoded on the GPU exactly as the benchmark
+    does; 3000 sampled frames (including both ends) checked on the oracle."""
+    w = ri.WORKLOAD_BY_NAME["large_batch"]
+    W = ri.make_weights(w)
+    Wt = ri.weights_to_torch(W, DEV)
+    xt = ri.make_x_torch(w, Wt, DEV)
+    rvq = make_rvq(W)
+    codes = rvq.encode(xt)
+    y = rvq.decode(codes)
+    torch.cuda.synchronize()
+    rows = np.sort(np.concatenate([np.random.default_rng(2).choice(w.N - 2, 2998, replace=False) + 1, [0, w.N - 1]]))
+    ridx = torch.from_numpy(rows).to(DEV)
+    x_s = xt[ridx].cpu().numpy()
+    x_rms = float(torch.sqrt(torch.mean(xt.double() ** 2)).item())
+    ref = oracle.encode(W, x_s, want_residual=False)
+    cg = codes[ridx].cpu().numpy()
+    res = compare_codes(cg, ref["codes"], ref["gap"])
+    assert res["n_fail"] == 0, res
+    y_ref, _ = oracle.decode(W, cg)
+    err = max_abs_rel_to_rms(y[ridx].cpu().numpy(), y_ref, x_rms)
+    assert err <= FLOAT_TOL, err
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def _small_weights(D=64, K=256, Q=4, seed=3, bias=False, decay=1.0):
+    w = ri.Workload("edge", 1, 1, D, Q, K, 64, "gauss", cb_decay=decay, seed=seed)
+    return w, ri.make_weights(w, with_bias=bias, bias_scale=0.3)
+
+
+@pytest.mark.parametrize("N", [1, 2, 63, 64, 65, 127, 129, 333])
+def test_ragged_frame_counts(N):
+    w, W = _small_weights(D=128, K=256, Q=3, seed=10 + N)
+    x = np.random.default_rng(N).standard_normal((N, 128)).astype(np.float32)
+    run_small(W, x, label=f"N={N}")
+
+
+@pytest.mark.parametrize("D,K,Q", [(16, 128, 1), (48, 128, 2), (256, 384, 5), (2048, 256, 2)])
+def test_other_shapes(D, K, Q):
+    w, W = _small_weights(D=D, K=K, Q=Q, seed=D + K + Q)
+    x = np.random.default_rng(D).standard_normal((300, D)).astype(np.float32)
+    run_small(W, x, label=f"D={D} K={K} Q={Q}")
+
+
+def test_biases_and_prefix_depths():
+    w, W = _small_weights(D=256, K=512, Q=6, bias=True)
+    x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
+    _, full = run_small(W, x, label="bias full")
+    for n_q in (1, 2, 5):
+        _, c = run_small(W, x, n_q=n_q, label=f"bias n_q={n_q}")
+        assert np.array_equal(c, full[:, :n_q]), "prefix property"
+
+
+def test_exact_ties_take_lowest_index():
+    """Duplicated codebook rows give bit-identical distances; the lower index
+    must win.  Frames sit right on duplicated entries."""
+    D, K, Q = 64, 256, 2
+    w, W = _small_weights(D=D, K=K, Q=Q, seed=77)
+    W["w_in"] = np.stack([np.eye(64, dtype=np.float32)] * Q)
+    W["w_out"] = np.stack([np.eye(64, dtype=np.float32)] * Q)
+    rng = np.random.default_rng(8)
+    for q in range(Q):
+        for lo, hi in ((3, 200), (17, 18), (100, 255)):
+            W["codebook"][q, hi] = W["codebook"][q, lo]
+    picks = np.array([3, 200, 17, 18, 100, 255] * 20)
+    x = W["codebook"][0][picks] + 0.01 * rng.standard_normal((len(picks), D)).astype(np.float32)
+    x = x.astype(np.float32)
+    rvq = make_rvq(W)
+    codes = rvq.encode(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    ref = oracle.encode(W, x)
+    assert np.array_equal(codes[:, 0], ref["codes"][:, 0])
+    assert set(codes[:, 0].tolist()) <= {3, 17, 100}
+
+
+def test_small_scratch_chunks_agree_bitwise():
+    w = ri.WORKLOAD_BY_NAME["tiny"]
+    W = ri.make_weights(w)
+    x = torch.from_numpy(ri.make_x(w, W)).to(DEV)
+    rvq = make_rvq(W)
+    c_big = rvq.encode(x)
+    small = torch.empty(rq.rvq_encode_min_scratch_bytes(rvq.dims, 8), dtype=torch.uint8, device=DEV)
+    c_small = torch.empty_like(c_big)
+    rq.rvq_encode(rvq.dims, rvq.tables, x, 8, c_small, small)
+    torch.cuda.synchronize()
+    assert torch.equal(c_big, c_small)
+
+
+def test_decode_counts_bad_codes():
+    w, W = _small_weights(D=64, K=128, Q=3)
+    rvq = make_rvq(W)
+    codes = np.array([[1, 2, 3], [-1, 5, 128], [127, 1 << 30, 0]], dtype=np.int32)
+    bad = torch.zeros(1, dtype=torch.int64, device=DEV)
+    y = rvq.decode(torch.from_numpy(codes).to(DEV), bad_codes=bad).cpu().numpy()
+    assert int(bad.item()) == 3
+    y_ref, n_bad = oracle.decode(W, codes)
+    assert n_bad == 3
+    assert max_abs_rel_to_rms(y, y_ref, 1.0) <= 1e-5
+
+
+def test_empty_batch_and_determinism():
+    w = ri.WORKLOAD_BY_NAME["tiny"]
+    W = ri.make_weights(w)
+    rvq = make_rvq(W)
+    empty = torch.empty((0, w.D), dtype=torch.float32, device=DEV)
+    assert rvq.encode(empty).shape == (0, 8)
+    x = torch.from_numpy(ri.make_x(w, W)).to(DEV)
+    a = rvq.reconstruct(x)
+    b = rvq.reconstruct(x)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_invalid_arguments_raise():
+    w, W = _small_weights()
+    rvq = make_rvq(W)
+    x = torch.zeros((4, 64), device=DEV)
+    with pytest.raises(rq.RVQError):
+        rvq.encode(x, n_q=5)
+    with pytest.raises(ValueError):
+        rvq.encode(torch.zeros((4, 65), device=DEV))
