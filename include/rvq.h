@@ -157,6 +157,23 @@ RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const floa
                                    int64_t n_frames, int32_t n_q, int32_t *codes, float *x_hat,
                                    void *scratch, size_t scratch_bytes, rvq_stream_t stream);
 
+/* Encode like rvq_encode, but with no scratch argument: for callers that
+ * cannot allocate device memory when they encode (a real-time audio callback,
+ * where cudaMalloc may stall on device-wide synchronisation, or an application
+ * whose device memory all belongs to its own pool).  The pages have no
+ * counterpart to this entry point.
+ * Scratch is a fixed RVQ_STATIC_SCRATCH_BYTES array inside the library, held
+ * on every GPU that loads it until the process exits.  A call needs
+ * n_frames * n_q * d * 4 bytes of it; a larger call returns RVQ_ERR_WORKSPACE
+ * before launching anything (split the frames over several calls).  The
+ * first call on each device looks up the array's device address, so make it
+ * before any stream capture.  All calls share the array: calls that can
+ * overlap on the GPU race and must not be issued.  Allocates nothing. */
+#define RVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const float *x,
+                                     int64_t n_frames, int32_t n_q, int32_t *codes,
+                                     rvq_stream_t stream);
+
 /* Static strings. */
 RVQ_API const char *rvq_status_string(rvq_status status);
 RVQ_API const char *rvq_version(void);

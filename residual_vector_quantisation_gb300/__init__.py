@@ -28,7 +28,8 @@ __all__ = [
     "RVQError", "load_library", "library_path", "rvq_dims", "rvq_weights",
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
-    "rvq_status_string", "rvq_version", "RVQ", "EXPORTED_SYMBOLS",
+    "rvq_status_string", "rvq_version", "rvq_encode_static", "RVQ_STATIC_SCRATCH_BYTES", "RVQ",
+    "EXPORTED_SYMBOLS",
 ]
 
 RVQ_OK = 0
@@ -38,8 +39,10 @@ STATUS_NAMES = {0: "RVQ_OK", -1: "RVQ_ERR_INVALID_ARG", -2: "RVQ_ERR_UNSUPPORTED
 EXPORTED_SYMBOLS = [
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
-    "rvq_status_string", "rvq_version",
+    "rvq_status_string", "rvq_version", "rvq_encode_static",
 ]
+
+RVQ_STATIC_SCRATCH_BYTES = 16 << 20  # include/rvq.h
 
 
 class RVQError(RuntimeError):
@@ -86,6 +89,7 @@ def load_library(path: Optional[str] = None):
         "rvq_reconstruct": ([rvq_dims, vp, vp, i64, i32, vp, vp, vp, sz, vp], ctypes.c_int),
         "rvq_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "rvq_version": ([], ctypes.c_char_p),
+        "rvq_encode_static": ([rvq_dims, vp, vp, i64, i32, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -166,6 +170,13 @@ def rvq_reconstruct(dims: rvq_dims, tables, x, n_q: int, codes, x_hat, scratch, 
                                                              _ptr(x_hat), _ptr(scratch),
                                                              scratch.numel() * scratch.element_size(),
                                                              _stream(stream)))
+
+
+def rvq_encode_static(dims: rvq_dims, tables, x, n_q: int, codes, stream=None) -> None:
+    """Encode with the library's own fixed scratch (no scratch argument; see rvq.h)."""
+    n = x.shape[0]
+    _check("rvq_encode_static", load_library().rvq_encode_static(dims, _ptr(tables), _ptr(x), n, int(n_q),
+                                                                 _ptr(codes), _stream(stream)))
 
 
 def rvq_status_string(status: int) -> str:
