@@ -178,7 +178,11 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = ri.WORKLOAD_BY_NAME[WORKLOAD]
+    w = ri.WORKLOAD_BY_NAME[args.workload]
+    if w.kind != "planted" and w.kind != "gauss":
+        raise SystemExit("bench needs a workload with frames (encode + decode)")
+    if args.frames and args.frames < w.N:  # a smaller case of the same workload (profiling)
+        w = ri.Workload(w.name, 1, args.frames, w.D, w.Q, w.K, w.d, w.kind, w.sigma, w.cb_decay, w.seed)
     W = ri.make_weights(w)
     Wt = ri.weights_to_torch(W, dev)
     rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev)
@@ -227,7 +231,19 @@ def run_ours(args):
     enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
 
-    # end to end through the public API: pinned host frames in, host codes + reconstruction out
+    e2e_ms = None
+    if not args.no_e2e:
+        e2e_ms = e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev)
+
+    if rank == 0:
+        report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, clocks, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev):
+    """Same step through the public API: pinned host frames in, host codes and y out."""
+    import torch
     x_host = x.cpu().pin_memory()
     codes_host = torch.empty(codes.shape, dtype=codes.dtype, pin_memory=True)
     y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
@@ -255,49 +271,113 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    return e2e_ms
 
-    if rank == 0:
-        peaks = _peaks()
-        clk = clocks.summary()
-        # encode: FP32 SIMT kernels; the ALU peak is SMs x 128 lanes x 2 FLOP x max SM clock
-        fp32_peak_tflops = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-        enc_achieved = encode_flops_per_frame(w) * N / (enc_ms / 1e3) / 1e12
-        dec_achieved = decode_bytes_per_frame(w) * N / (dec_ms / 1e3) / 1e9
-        scratch_rows = scratch.numel() // (n_q * w.d * 4)
-        chunk = N if scratch_rows >= N else scratch_rows // 128 * 128
-        n_chunks = math.ceil(N / chunk)
-        launches_per_step = 2 * n_chunks + 1
-        cpu = None
-        if world == 1 and not args.no_cpu_baseline:
-            rows = args.cpu_frames
-            cpu = cpu_baseline_leg(W, x[:rows].cpu().numpy(), w)
-        value = world * N / (ms_step / 1e3)
-        out = {
-            "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.describe(), "frames_per_gpu": N, "parallelism": f"replicas{world}",
-                       "l2": "inputs and outputs larger than L2 (786 MB each); no flush",
-                       "step": "rvq_encode + rvq_decode through the C ABI"},
-            "encode_ms": enc_ms, "decode_ms": dec_ms,
-            "encode_frames_per_s": N / (enc_ms / 1e3), "decode_frames_per_s": N / (dec_ms / 1e3),
-            "roofline": {"bound": "alu", "achieved": enc_achieved, "peak": fp32_peak_tflops, "unit": "TFLOP/s",
-                         "frac": enc_achieved / fp32_peak_tflops, "traffic": None,
-                         "kernel": "encode (projection GEMM + stage search, FP32 SIMT)",
-                         "peak_basis": f"{SM_COUNT} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x "
-                                       f"{peaks['sm_max_mhz']:.0f} MHz"},
-            "roofline_decode": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": dec_achieved / peaks["hbm_gbs"], "traffic": None,
-                                "peak_basis": f"{peaks['source']} HBM copy bandwidth"},
-            "cpu_baseline": cpu,
-            "e2e": {"value": world * N / (e2e_ms / 1e3), "unit": "frames/s",
-                    "h2d_bytes_per_step": N * w.D * 4, "d2h_bytes_per_step": N * w.D * 4 + N * n_q * 4},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
-        }
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+
+def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, clocks, world):
+    peaks = _peaks()
+    clk = clocks.summary()
+    # encode: 3xTF32 tensor-core kernels.  The TF32 peak is the measured bf16
+    # peak times the nominal dense tf32/bf16 ratio (1.1 / 2.25 PFLOP/s); three
+    # TF32 passes make up one float32-accurate product, so the roofline for the
+    # algorithmic FLOPs is a third of it.
+    tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+    tc_peak = tf32_peak / 3.0
+    enc_achieved = encode_flops_per_frame(w) * N / (enc_ms / 1e3) / 1e12
+    dec_achieved = decode_bytes_per_frame(w) * N / (dec_ms / 1e3) / 1e9
+    scratch_rows = (scratch.numel() - 256) // (n_q * w.d * 4)
+    chunk = N if scratch_rows >= N else scratch_rows // 128 * 128
+    wave = 256 * SM_COUNT
+    if chunk < N and chunk >= wave:
+        chunk = chunk // wave * wave
+    n_chunks = math.ceil(N / chunk)
+    launches_per_step = 2 * n_chunks + 1
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rows = args.cpu_frames
+        cpu = cpu_baseline_leg(W, x[:rows].cpu().numpy(), w)
+    value = world * N / (ms_step / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.describe(), "frames_per_gpu": N, "parallelism": f"replicas{world}",
+                   "l2": (f"input and output {N * w.D * 4 / 1e6:.0f} MB each, "
+                         + ("larger than L2; no flush" if N * w.D * 4 > L2_BYTES else "L2-resident (profiling case)")),
+                   "step": "rvq_encode + rvq_decode through the C ABI"},
+        "encode_ms": enc_ms, "decode_ms": dec_ms,
+        "encode_frames_per_s": N / (enc_ms / 1e3), "decode_frames_per_s": N / (dec_ms / 1e3),
+        "roofline": {"bound": "tensor", "achieved": enc_achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": enc_achieved / tc_peak, "traffic": None,
+                     "kernel": "encode: k_project_tc + k_search_tc (3xTF32 tcgen05), algorithmic FLOPs "
+                               "Q*(2*D*d + 2*K*d) per frame",
+                     "peak_basis": f"{peaks['source']} bf16 {peaks['bf16_tflops']:.1f} x 1.1/2.25 (tf32) / 3 passes",
+                     "frac_of_single_pass_tf32": enc_achieved / tf32_peak},
+        "roofline_decode": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": dec_achieved / peaks["hbm_gbs"], "traffic": None,
+                            "peak_basis": f"{peaks['source']} HBM copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": None if e2e_ms is None else {
+            "value": world * N / (e2e_ms / 1e3), "unit": "frames/s",
+            "h2d_bytes_per_step": N * w.D * 4, "d2h_bytes_per_step": N * w.D * 4 + N * n_q * 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def measure_peaks():
+    """Machine figures the rooflines need: cuBLAS TF32 and FP32 GEMM rates,
+    L2 read bandwidth and L2 row-gather bandwidth (CUDA events, best of 10)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    out = {}
+
+    def best(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        return min(ts)
+
+    n = 8192
+    A = torch.randn(n, n, device=dev)
+    B = torch.randn(n, n, device=dev)
+    C = torch.empty(n, n, device=dev)
+    for name, tf32 in (("tf32_tflops", True), ("fp32_cublas_tflops", False)):
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+        t = best(lambda: torch.matmul(A, B, out=C), reps=5)
+        out[name] = 2.0 * n ** 3 / t / 1e12
+    torch.backends.cuda.matmul.allow_tf32 = False
+    del A, B, C
+    # L2 read bandwidth: sum a 32 MiB buffer repeatedly (stays L2-resident)
+    buf = torch.randn(8 << 20, device=dev)
+    acc = torch.empty((), device=dev)
+    t = best(lambda: [torch.sum(buf, dim=0, out=acc) for _ in range(50)])
+    out["l2_read_gbs"] = 50 * buf.numel() * 4 / t / 1e9
+    # L2 gather: rows of 4 KB from a 32 MiB table (the decode table's shape)
+    table = torch.randn(8192, 1024, device=dev)
+    idx = torch.randint(0, 8192, (65536,), device=dev)
+    dst = torch.empty(65536, 1024, device=dev)
+    t = best(lambda: torch.index_select(table, 0, idx, out=dst))
+    out["gather_4kb_rows_gbs_read"] = 65536 * 4096 / t / 1e9
+    out["gather_4kb_rows_gbs_read_plus_write"] = 2 * 65536 * 4096 / t / 1e9
+    # HBM copy for reference
+    big_a = torch.empty(1 << 28, device=dev)
+    big_b = torch.empty_like(big_a)
+    t = best(lambda: big_b.copy_(big_a))
+    out["hbm_copy_gbs"] = 2 * big_a.numel() * 4 / t / 1e9
+    props = torch.cuda.get_device_properties(dev)
+    out["sm_count"] = props.multi_processor_count
+    out["l2_bytes"] = getattr(props, "L2_cache_size", None)
+    out["name"] = props.name
+    print(json.dumps(out), flush=True)
 
 
 def main():
@@ -309,9 +389,15 @@ def main():
     ap.add_argument("--cpu-frames", type=int, default=49152, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-frames", type=int, default=8192, help="oracle frames per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[w.name for w in ri.WORKLOADS])
+    ap.add_argument("--frames", type=int, default=0, help="use only the first N frames (profiling)")
+    ap.add_argument("--peaks", action="store_true", help="measure TF32/FP32 GEMM and L2 bandwidths instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
-    if args.impl == "reference":
+    if args.peaks:
+        measure_peaks()
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

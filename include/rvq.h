@@ -125,11 +125,15 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
                                size_t tables_bytes, rvq_stream_t stream);
 
 /* Scratch bytes rvq_encode / rvq_reconstruct need for n_frames frames at
- * depth n_q.  Encode works through the frames in chunks whose per-frame stage
- * projections ([chunk][n_q*d] float32) live in scratch; this returns the size
- * that lets one chunk cover up to a bounded number of frames (about 32 MiB).
- * A larger scratch is accepted and used for larger chunks; a smaller one (at
- * least rvq_encode_min_scratch_bytes) gives smaller chunks. */
+ * depth n_q.  Scratch starts with a 256-byte header whose first int32 is a
+ * device status word: each call sets it to 0, and a kernel sets it to 5 if
+ * one of its bounded device waits gave up (that call's codes are then
+ * invalid; read it after the stream reaches the call).  The rest holds the
+ * per-frame stage projections ([chunk][n_q*d] float32) of one chunk of
+ * frames; encode works through the frames chunk by chunk.  This returns the
+ * size for chunks of up to about 96 MiB of projections.  A larger scratch is
+ * accepted and used for larger chunks; a smaller one (at least
+ * rvq_encode_min_scratch_bytes) gives smaller chunks. */
 RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q);
 RVQ_API size_t rvq_encode_min_scratch_bytes(rvq_dims dims, int32_t n_q);
 
@@ -164,7 +168,7 @@ RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const floa
  * counterpart to this entry point.
  * Scratch is a fixed RVQ_STATIC_SCRATCH_BYTES array inside the library, held
  * on every GPU that loads it until the process exits.  A call needs
- * n_frames * n_q * d * 4 bytes of it; a larger call returns RVQ_ERR_WORKSPACE
+ * 256 + n_frames * n_q * d * 4 bytes of it; a larger call returns RVQ_ERR_WORKSPACE
  * before launching anything (split the frames over several calls).  The
  * first call on each device looks up the array's device address, so make it
  * before any stream capture.  All calls share the array: calls that can

@@ -7,15 +7,12 @@
 
 #include "rvq_internal.cuh"
 
-namespace rvq {
-size_t search_smem_bytes(int n_q);
-}
 
 namespace {
 
 using rvq::TablesLayout;
 
-constexpr size_t kChunkTargetBytes = size_t(32) << 20;  // projections per encode chunk (L2-resident)
+constexpr size_t kChunkTargetBytes = size_t(96) << 20;  // projections per encode chunk
 constexpr int64_t kChunkQuantum = 128;                   // frames
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -35,7 +32,8 @@ size_t row_bytes(const rvq_dims &dm, int32_t n_q) { return (size_t)n_q * dm.d * 
 // Frames per encode chunk for a given scratch size (0 if the scratch is too small).
 int64_t chunk_frames(const rvq_dims &dm, int32_t n_q, int64_t n_frames, size_t scratch_bytes) {
   const size_t rb = row_bytes(dm, n_q);
-  int64_t fit = (int64_t)(scratch_bytes / rb);
+  if (scratch_bytes <= rvq::kScratchHeader) return 0;
+  int64_t fit = (int64_t)((scratch_bytes - rvq::kScratchHeader) / rb);
   if (fit >= n_frames) return n_frames;
   fit = fit / kChunkQuantum * kChunkQuantum;
   return fit;
@@ -43,12 +41,26 @@ int64_t chunk_frames(const rvq_dims &dm, int32_t n_q, int64_t n_frames, size_t s
 
 rvq_status launch_status(cudaError_t e) { return e == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA; }
 
+int device_sms() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      v <= 0)
+    return 1;
+  return v;
+}
+
 rvq_status encode_impl(const rvq_dims &dm, const void *tables, const float *x, int64_t n_frames, int32_t n_q,
                        int32_t *codes, void *scratch, size_t scratch_bytes, cudaStream_t st) {
-  const int64_t chunk = chunk_frames(dm, n_q, n_frames, scratch_bytes);
+  int64_t chunk = chunk_frames(dm, n_q, n_frames, scratch_bytes);
+  // a chunk of whole waves: one 256-frame search item per SM
+  const int64_t wave = 256 * (int64_t)device_sms();
+  if (chunk < n_frames && chunk >= wave) chunk = chunk / wave * wave;
+  int *status = static_cast<int *>(scratch);
+  float *p0 = reinterpret_cast<float *>(static_cast<char *>(scratch) + rvq::kScratchHeader);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return RVQ_ERR_CUDA;
   for (int64_t n0 = 0; n0 < n_frames; n0 += chunk) {
     const int64_t n = (n_frames - n0 < chunk) ? n_frames - n0 : chunk;
-    cudaError_t e = rvq::launch_encode_chunk(dm, tables, x, n0, n, n_q, codes, static_cast<float *>(scratch), st);
+    cudaError_t e = rvq::launch_encode_chunk(dm, tables, x, n0, n, n_q, codes, p0, status, st);
     if (e != cudaSuccess) return RVQ_ERR_CUDA;
   }
   return RVQ_OK;
@@ -91,7 +103,7 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
 
 RVQ_API size_t rvq_encode_min_scratch_bytes(rvq_dims dims, int32_t n_q) {
   if (check_dims(dims) != RVQ_OK || n_q < 1 || n_q > dims.Q) return 0;
-  return (size_t)kChunkQuantum * row_bytes(dims, n_q);
+  return rvq::kScratchHeader + (size_t)kChunkQuantum * row_bytes(dims, n_q);
 }
 
 RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q) {
@@ -100,7 +112,7 @@ RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t
   int64_t target = (int64_t)(kChunkTargetBytes / rb) / kChunkQuantum * kChunkQuantum;
   if (target < kChunkQuantum) target = kChunkQuantum;
   const int64_t frames = n_frames < target ? (n_frames > 0 ? n_frames : 1) : target;
-  return (size_t)frames * rb;
+  return rvq::kScratchHeader + (size_t)frames * rb;
 }
 
 RVQ_API rvq_status rvq_encode(rvq_dims dims, const void *tables, const float *x, int64_t n_frames, int32_t n_q,

@@ -12,8 +12,9 @@
 // The buffer is a file-scope __device__ array of RVQ_STATIC_SCRATCH_BYTES
 // (16 MiB, declared in rvq.h).
 // Every GPU that loads the library holds one copy until the process exits.
-// A call needs n_frames * n_q * d * 4 bytes of it; larger calls are refused
-// with RVQ_ERR_WORKSPACE before anything is launched.
+// A call needs 256 + n_frames * n_q * d * 4 bytes of it (a status word, then
+// the stage projections); larger calls are refused with RVQ_ERR_WORKSPACE
+// before anything is launched.
 //
 // The array's address is looked up with cudaGetSymbolAddress once per device
 // (with that device current), on the first call made on that device; make
@@ -70,12 +71,15 @@ extern "C" RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *table
   if ((reinterpret_cast<uintptr_t>(tables) & 255u) || (reinterpret_cast<uintptr_t>(x) & 15u) ||
       (reinterpret_cast<uintptr_t>(codes) & 15u))
     return RVQ_ERR_INVALID_ARG;
-  const size_t need = (size_t)n_frames * (size_t)n_q * (size_t)dims.d * sizeof(float);
+  const size_t need = rvq::kScratchHeader + (size_t)n_frames * (size_t)n_q * (size_t)dims.d * sizeof(float);
   if (need > kStaticScratchBytes) return RVQ_ERR_WORKSPACE;
   void *scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) return RVQ_ERR_CUDA;
-  cudaError_t e = rvq::launch_encode_chunk(dims, tables, x, 0, n_frames, n_q, codes,
-                                           static_cast<float *>(scratch),
-                                           reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int *status = static_cast<int *>(scratch);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return RVQ_ERR_CUDA;
+  cudaError_t e = rvq::launch_encode_chunk(
+      dims, tables, x, 0, n_frames, n_q, codes,
+      reinterpret_cast<float *>(static_cast<char *>(scratch) + rvq::kScratchHeader), status, st);
   return e == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA;
 }

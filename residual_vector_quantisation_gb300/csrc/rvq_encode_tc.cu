@@ -1,0 +1,575 @@
+// RVQ encode on the fifth-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// The encode loop of omnivoice.cpp ARCHITECTURE.md ("RVQ codec", Encode
+// (residual loop)) in the re-associated form prepared by rvq_prepare:
+//
+//   step 1 (k_project_tc)  P0[n][q*d + j] = w_in[q][j] . x[n] + b_in[q][j]   for all q < n_q
+//   step 2 (k_search_tc)   for q = 0 .. n_q-1, per frame:
+//                            p_q    = P0[n][q] - sum_{s<q} G[q][s][code_s]
+//                            code_q = argmin_k  ||c_k||^2 - 2 p_q . c_k   (lowest k on ties)
+//
+// Both contractions run as 3xTF32 on the tensor cores: a = a_hi + a_lo with
+// a_hi the TF32 truncation (the tensor core truncates float32 operands to TF32,
+// so a raw float32 tile serves as a_hi) and a_lo = a - a_hi exact in float32;
+// a.b ~= a_hi.b_hi + a_hi.b_lo + a_lo.b_hi, accumulated in float32 in TMEM.
+// That keeps the distances at about float32 accuracy; one TF32 pass (10-bit
+// mantissa) would not (the pages keep the codec in F32 because reduced
+// precision loses late-codebook matches: omnivoice.cpp ARCHITECTURE.md,
+// "Model conversion").
+//
+// Every mbarrier wait is bounded; a timeout records RVQ_DEVICE_TIMEOUT in the
+// scratch status word, the kernel drains its own copies and MMAs, frees TMEM
+// and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "rvq_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace rvq {
+namespace {
+
+using namespace ptx;
+
+// ===========================================================================
+// step 1: P0 = x . w_in^T + b_in
+// CTA item: 256 frames (two M=128 tiles) x 256 output columns, K = D in
+// slices of 16 floats (64-byte rows, 64-byte swizzle), 3-stage TMA ring.
+// Warps: 0 TMA producer, 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
+// ===========================================================================
+constexpr int PJ_BK = 16;
+constexpr int PJ_STAGES = 3;
+constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;          // 8 KB: one tile's K-slice
+constexpr uint32_t PJ_B = 256 * PJ_BK * 4;               // 16 KB
+constexpr uint32_t PJ_STAGE = 4 * PJ_A_TILE + 2 * PJ_B;  // raw[2] lo[2] bhi blo = 64 KB
+constexpr uint32_t PJ_TX = 2 * PJ_A_TILE + 2 * PJ_B;     // bytes TMA writes per stage
+constexpr int PJ_THREADS = 192;
+constexpr uint32_t PJ_IDESC = idesc_tf32(128, 256);
+
+struct PjBars {
+  uint64_t full[PJ_STAGES], conv[PJ_STAGES], empty[PJ_STAGES];
+  uint64_t acc_full, acc_empty, drain;
+  uint32_t tmem;
+};
+constexpr size_t PJ_SMEM = 1024 + PJ_STAGES * PJ_STAGE + sizeof(PjBars);
+
+__device__ __forceinline__ void record_error(int *status, int code) { atomicCAS(status, 0, code); }
+
+__global__ void __launch_bounds__(PJ_THREADS, 1)
+    k_project_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_whi,
+                 const __grid_constant__ CUtensorMap tm_wlo, const float *__restrict__ bias,
+                 float *__restrict__ P0, int64_t n_rows, int n_cols, int D, int n_items, int n_cb,
+                 int *__restrict__ status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
+  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * PJ_STAGE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nk = D / PJ_BK;
+  auto a_raw = [&](int s, int t) { return smem + s * PJ_STAGE + t * PJ_A_TILE; };
+  auto a_lo = [&](int s, int t) { return smem + s * PJ_STAGE + (2 + t) * PJ_A_TILE; };
+  auto b_hi = [&](int s) { return smem + s * PJ_STAGE + 4 * PJ_A_TILE; };
+  auto b_lo = [&](int s) { return smem + s * PJ_STAGE + 4 * PJ_A_TILE + PJ_B; };
+
+  if (tid == 0) {
+    for (int s = 0; s < PJ_STAGES; ++s) {
+      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.conv[s], 128);
+      mbar_init(&bar.empty[s], 1);
+    }
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.acc_empty, 128);
+    mbar_init(&bar.drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_whi);
+    prefetch_tmap(&tm_wlo);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int m0 = (item / n_cb) * 256, c0 = (item % n_cb) * 256;
+        for (int ks = 0; ks < nk; ++ks, ++it) {
+          const int s = it % PJ_STAGES;
+          const uint32_t use = it / PJ_STAGES;
+          if (use > 0 && !mbar_wait(&bar.empty[s], (use - 1) & 1)) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar.full[s], PJ_TX);
+          tma_load_2d(a_raw(s, 0), &tm_x, ks * PJ_BK, m0, &bar.full[s]);
+          tma_load_2d(a_raw(s, 1), &tm_x, ks * PJ_BK, m0 + 128, &bar.full[s]);
+          tma_load_2d(b_hi(s), &tm_whi, ks * PJ_BK, c0, &bar.full[s]);
+          tma_load_2d(b_lo(s), &tm_wlo, ks * PJ_BK, c0, &bar.full[s]);
+        }
+      }
+      // drain: the last load issued into each stage has landed before exit
+      for (uint32_t k = 0; k < PJ_STAGES && k < it; ++k) {
+        const uint32_t j = it - 1 - k;
+        mbar_wait(&bar.full[j % PJ_STAGES], (j / PJ_STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, n_done = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n_done) {
+        if (n_done > 0 && !mbar_wait(&bar.acc_empty, (n_done - 1) & 1)) {
+          record_error(status, RVQ_DEVICE_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < nk; ++ks, ++it) {
+          const int s = it % PJ_STAGES;
+          if (!mbar_wait(&bar.conv[s], (it / PJ_STAGES) & 1)) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int j = 0; j < PJ_BK / 8; ++j) {
+              const uint64_t ah = smem_desc(smem_addr(a_raw(s, t)) + j * 32, 16, 512, kSwizzle64B);
+              const uint64_t al = smem_desc(smem_addr(a_lo(s, t)) + j * 32, 16, 512, kSwizzle64B);
+              const uint64_t bh = smem_desc(smem_addr(b_hi(s)) + j * 32, 16, 512, kSwizzle64B);
+              const uint64_t bl = smem_desc(smem_addr(b_lo(s)) + j * 32, 16, 512, kSwizzle64B);
+              const uint32_t d = tmem + t * 256;
+              mma_tf32(d, ah, bh, PJ_IDESC, (ks | j) ? 1u : 0u);
+              mma_tf32(d, ah, bl, PJ_IDESC, 1u);
+              mma_tf32(d, al, bh, PJ_IDESC, 1u);
+            }
+          mma_commit(&bar.empty[s]);
+        }
+        if (ok) mma_commit(&bar.acc_full);
+      }
+      // no MMA of this CTA may be in flight when TMEM is freed
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0);
+    }
+  } else {
+    // ---------------- lo split + epilogue (warps 2..5) ----------------
+    const int ct = tid - 64;                 // 0..127
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;       // row within each tile
+    uint32_t it = 0, n_done = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n_done) {
+      const int64_t m0 = (int64_t)(item / n_cb) * 256;
+      const int c0 = (item % n_cb) * 256;
+      for (int ks = 0; ks < nk; ++ks, ++it) {
+        const int s = it % PJ_STAGES;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.full[s], (it / PJ_STAGES) & 1))) {
+          record_error(status, RVQ_DEVICE_TIMEOUT);
+          ok = false;
+          break;
+        }
+        // lo = a - trunc_tf32(a), element-wise over both tiles' raw slices
+        const float4 *src = reinterpret_cast<const float4 *>(a_raw(s, 0));
+        float4 *dst = reinterpret_cast<float4 *>(a_lo(s, 0));
+#pragma unroll
+        for (int u = 0; u < (2 * PJ_A_TILE / 16) / 128; ++u) {
+          const float4 v = src[ct + u * 128];
+          float4 l;
+          l.x = v.x - __uint_as_float(__float_as_uint(v.x) & 0xffffe000u);
+          l.y = v.y - __uint_as_float(__float_as_uint(v.y) & 0xffffe000u);
+          l.z = v.z - __uint_as_float(__float_as_uint(v.z) & 0xffffe000u);
+          l.w = v.w - __uint_as_float(__float_as_uint(v.w) & 0xffffe000u);
+          dst[ct + u * 128] = l;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.conv[s]);
+      }
+      if (!ok) break;
+      // warp-uniform decision before the warp-collective TMEM loads
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full, n_done & 1))) {
+        record_error(status, RVQ_DEVICE_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        const int64_t n = m0 + t * 128 + r;
+        float *out = P0 + n * n_cols + c0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + t * 256 + c, v);
+          tmem_wait_ld();
+          if (n < n_rows && c0 + c < n_cols) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0 + c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 b = __ldg(b4 + u);
+              reinterpret_cast<float4 *>(out + c)[u] =
+                  make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.acc_empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// step 2: the stage loop in code space.
+// CTA item: 256 frames as two M=128 tiles that walk the stages in lockstep
+// and share every codebook chunk.  Chunk = 128 codewords; its -2*c hi and lo
+// halves arrive as two 32 KB bulk copies of pre-swizzled images.  Per chunk
+// and tile the accumulator is 128 lanes x 128 columns of TMEM, double
+// buffered so the argmin of chunk c overlaps the MMAs of chunk c+1.
+// Warps: 0 bulk-copy producer, 1 MMA issuer (+ TMEM owner), 2-9 one thread
+// per frame row: build the stage's query p_q, then scan the distances.
+// ===========================================================================
+constexpr int SR_KC = 128;
+constexpr int SR_STAGES = 3;
+constexpr uint32_t SR_ATOM = 128 * 128;            // 128 rows x 128 B
+constexpr uint32_t SR_A_BYTES = 2 * 2 * 2 * SR_ATOM;  // [tile][hi,lo][atom] = 128 KB
+constexpr uint32_t SR_B_STAGE = 2 * SR_ATOM;          // [atom] = 32 KB
+constexpr int SR_THREADS = 320;
+constexpr uint32_t SR_IDESC = idesc_tf32(128, SR_KC);
+
+struct SrBars {
+  uint64_t b_full[SR_STAGES], b_empty[SR_STAGES];
+  uint64_t a_ready[2];
+  uint64_t acc_full[2][2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem;
+};
+constexpr size_t SR_SMEM = 1024 + SR_A_BYTES + SR_STAGES * SR_B_STAGE + sizeof(SrBars);
+
+__global__ void __launch_bounds__(SR_THREADS, 1)
+    k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
+                const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
+                int n_items, int *__restrict__ status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
+  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_A_BYTES + SR_STAGES * SR_B_STAGE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nkc = K / SR_KC;
+  constexpr int d = kCodeDim;
+  auto a_tile = [&](int t, int hl, int atom) { return smem + ((t * 2 + hl) * 2 + atom) * SR_ATOM; };
+  auto b_stage = [&](int s, int atom) { return smem + SR_A_BYTES + s * SR_B_STAGE + atom * SR_ATOM; };
+
+  if (tid == 0) {
+    for (int s = 0; s < SR_STAGES; ++s) {
+      mbar_init(&bar.b_full[s], 1);
+      mbar_init(&bar.b_empty[s], 1);
+    }
+    mbar_init(&bar.a_ready[0], 128);
+    mbar_init(&bar.a_ready[1], 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar.acc_full[b][0], 1);
+      mbar_init(&bar.acc_full[b][1], 1);
+      mbar_init(&bar.acc_empty[b], 256);
+    }
+    mbar_init(&bar.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem;
+
+  if (warp == 0) {
+    // ---------------- producer: codebook chunk images ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
+        for (int q = 0; q < n_q && ok; ++q)
+          for (int c = 0; c < nkc && ok; ++c)
+            for (int h = 0; h < 2; ++h, ++it) {
+              const int s = it % SR_STAGES;
+              const uint32_t use = it / SR_STAGES;
+              if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
+                record_error(status, RVQ_DEVICE_TIMEOUT);
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&bar.b_full[s], SR_B_STAGE);
+              const float *src = cb_img + ((((size_t)q * nkc + c) * 2 + h) * SR_B_STAGE) / 4;
+              bulk_g2s(b_stage(s, 0), src, SR_B_STAGE, &bar.b_full[s]);
+            }
+      for (uint32_t k = 0; k < SR_STAGES && k < it; ++k) {
+        const uint32_t j = it - 1 - k;
+        mbar_wait(&bar.b_full[j % SR_STAGES], (j / SR_STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, cc = 0, builds = 0;
+      bool ok = true;
+      auto wait_or_fail = [&](uint64_t *b, uint32_t parity) {
+        if (!mbar_wait(b, parity)) {
+          record_error(status, RVQ_DEVICE_TIMEOUT);
+          ok = false;
+        }
+        return ok;
+      };
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
+        for (int q = 0; q < n_q && ok; ++q, ++builds)
+          for (int c = 0; c < nkc && ok; ++c, ++cc) {
+            const int b = cc & 1;
+            const uint32_t use = cc >> 1;
+            if (use > 0 && !wait_or_fail(&bar.acc_empty[b], (use - 1) & 1)) break;
+            // hi half: a_hi . b_hi + a_lo . b_hi
+            int s = it % SR_STAGES;
+            if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t) {
+              if (c == 0 && !wait_or_fail(&bar.a_ready[t], builds & 1)) break;
+              tc_fence_after();
+              const uint32_t dt = tmem + b * 256 + t * SR_KC;
+#pragma unroll
+              for (int ks = 0; ks < d / 8; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                const uint64_t ah = smem_desc(smem_addr(a_tile(t, 0, ks >> 2)) + off, 16, 1024, kSwizzle128B);
+                const uint64_t al = smem_desc(smem_addr(a_tile(t, 1, ks >> 2)) + off, 16, 1024, kSwizzle128B);
+                const uint64_t bh = smem_desc(smem_addr(b_stage(s, ks >> 2)) + off, 16, 1024, kSwizzle128B);
+                mma_tf32(dt, ah, bh, SR_IDESC, ks ? 1u : 0u);
+                mma_tf32(dt, al, bh, SR_IDESC, 1u);
+              }
+            }
+            if (!ok) break;
+            mma_commit(&bar.b_empty[s]);
+            ++it;
+            // lo half: a_hi . b_lo
+            s = it % SR_STAGES;
+            if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t) {
+              const uint32_t dt = tmem + b * 256 + t * SR_KC;
+#pragma unroll
+              for (int ks = 0; ks < d / 8; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                const uint64_t ah = smem_desc(smem_addr(a_tile(t, 0, ks >> 2)) + off, 16, 1024, kSwizzle128B);
+                const uint64_t bl = smem_desc(smem_addr(b_stage(s, ks >> 2)) + off, 16, 1024, kSwizzle128B);
+                mma_tf32(dt, ah, bl, SR_IDESC, 1u);
+              }
+              mma_commit(&bar.acc_full[b][t]);
+            }
+            mma_commit(&bar.b_empty[s]);
+            ++it;
+          }
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0);
+    }
+  } else {
+    // ---------------- one thread per frame row (warps 2..9) ----------------
+    const int rt = tid - 64;            // 0..255
+    const int t = rt >> 7;              // tile
+    const int quarter = warp & 3;       // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;  // row within the tile
+    uint32_t cc = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int64_t n = (int64_t)item * 256 + t * 128 + r;
+      const bool valid = n < n_rows;
+      int32_t *crow = codes + (valid ? n : 0) * n_q;
+      for (int q = 0; q < n_q && ok; ++q) {
+        // ---- query p_q = P0[n][q] - sum_{s<q} G[q][s][code_s]
+        float p[d];
+        if (valid) {
+          const float4 *src = reinterpret_cast<const float4 *>(P0 + n * (int64_t)(n_q * d) + q * d);
+#pragma unroll
+          for (int u = 0; u < d / 4; ++u) *reinterpret_cast<float4 *>(&p[4 * u]) = src[u];
+          for (int s = 0; s < q; ++s) {
+            const float4 *g = reinterpret_cast<const float4 *>(G + (pair_index(q, s) * K + crow[s]) * d);
+#pragma unroll
+            for (int u = 0; u < d / 4; ++u) {
+              const float4 v = __ldg(g + u);
+              p[4 * u] -= v.x;
+              p[4 * u + 1] -= v.y;
+              p[4 * u + 2] -= v.z;
+              p[4 * u + 3] -= v.w;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < d; ++u) p[u] = 0.f;
+        }
+        // raw (= hi after TF32 truncation) and lo rows, 128-byte swizzled K-major
+#pragma unroll
+        for (int u = 0; u < d / 4; ++u) {
+          const int j = 4 * u;
+          const uint32_t off = sw128_offset(r, j & 31);
+          float4 h = make_float4(p[j], p[j + 1], p[j + 2], p[j + 3]);
+          float4 l;
+          l.x = h.x - __uint_as_float(__float_as_uint(h.x) & 0xffffe000u);
+          l.y = h.y - __uint_as_float(__float_as_uint(h.y) & 0xffffe000u);
+          l.z = h.z - __uint_as_float(__float_as_uint(h.z) & 0xffffe000u);
+          l.w = h.w - __uint_as_float(__float_as_uint(h.w) & 0xffffe000u);
+          *reinterpret_cast<float4 *>(a_tile(t, 0, j >> 5) + off) = h;
+          *reinterpret_cast<float4 *>(a_tile(t, 1, j >> 5) + off) = l;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.a_ready[t]);
+        // ---- scan the K distances ||c||^2 - 2 p.c in ascending k
+        float best_v = __int_as_float(0x7f800000);
+        int best_k = 0;
+        const float *cnq = cnorm + (int64_t)q * K;
+        for (int c = 0; c < nkc; ++c, ++cc) {
+          const int b = cc & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full[b][t], (cc >> 1) & 1))) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + b * 256 + t * SR_KC;
+#pragma unroll
+          for (int g = 0; g < SR_KC / 32; ++g) {
+            float v[32];
+            tmem_ld32(ta + g * 32, v);
+            tmem_wait_ld();
+            const float4 *cn4 = reinterpret_cast<const float4 *>(cnq + c * SR_KC + g * 32);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 cn = __ldg(cn4 + u);
+              const float e[4] = {v[4 * u] + cn.x, v[4 * u + 1] + cn.y, v[4 * u + 2] + cn.z, v[4 * u + 3] + cn.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (e[i] < best_v) {
+                  best_v = e[i];
+                  best_k = c * SR_KC + g * 32 + 4 * u + i;
+                }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bar.acc_empty[b]);
+        }
+        if (!ok) break;
+        if (valid) crow[q] = best_k;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// host side
+// ===========================================================================
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t tensor_map_2d(CUtensorMap *map, const float *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                          uint32_t box_outer, CUtensorMapSwizzle sw) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode_tiled) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * sizeof(float)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+std::atomic<unsigned long long> g_attr_done{0};
+
+cudaError_t ensure_attributes() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (g_attr_done.load() & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(k_project_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PJ_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_search_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  if (e != cudaSuccess) return e;
+  g_attr_done.fetch_or(bit);
+  return cudaSuccess;
+}
+
+int sm_count() {
+  static std::atomic<int> cached{0};
+  int v = cached.load();
+  if (v) return v;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+  cached.store(v);
+  return v;
+}
+
+}  // namespace
+
+cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0, int64_t n,
+                                int n_q, int32_t *codes, float *p0, int *status, cudaStream_t st) {
+  const TablesLayout L = tables_layout(dm);
+  const int D = dm.D, d = dm.d, K = dm.K, Q = dm.Q;
+  const int n_cols = n_q * d;
+  cudaError_t e = ensure_attributes();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_x, tm_whi, tm_wlo;
+  if ((e = tensor_map_2d(&tm_x, x + n0 * D, (uint64_t)D, (uint64_t)n, PJ_BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+      cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&tm_whi, at<float>(tables, L.w_in_hi), (uint64_t)D, (uint64_t)Q * d, PJ_BK, 256,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&tm_wlo, at<float>(tables, L.w_in_lo), (uint64_t)D, (uint64_t)Q * d, PJ_BK, 256,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+    return e;
+  const int n_pairs_rows = (int)((n + 255) / 256);
+  const int n_cb = (n_cols + 255) / 256;
+  const int items1 = n_pairs_rows * n_cb;
+  const int sms = sm_count();
+  k_project_tc<<<items1 < sms ? items1 : sms, PJ_THREADS, PJ_SMEM, st>>>(
+      tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_search_tc<<<n_pairs_rows < sms ? n_pairs_rows : sms, SR_THREADS, SR_SMEM, st>>>(
+      p0, at<float>(tables, L.g), at<float>(tables, L.cb_img), at<float>(tables, L.cnorm), codes + n0 * n_q, n, n_q,
+      K, n_pairs_rows, status);
+  return cudaGetLastError();
+}
+
+}  // namespace rvq

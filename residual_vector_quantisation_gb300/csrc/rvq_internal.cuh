@@ -10,7 +10,10 @@
 namespace rvq {
 
 constexpr int kCodeDim = 64;            // d supported by the kernels
-constexpr int kMaxStages = 64;
+constexpr int kChunkCodes = 128;        // codewords per tensor-core distance chunk
+constexpr size_t kScratchHeader = 256;  // status word at the head of encode scratch
+constexpr int RVQ_DEVICE_TIMEOUT = 5;   // status word value: a bounded device wait gave up
+constexpr int kMaxStages = 64;         // Q limit
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -21,13 +24,12 @@ __host__ __device__ inline int64_t pair_index(int q, int s) { return (int64_t)q 
 
 // Byte offsets of the prepared tables inside the caller's tables buffer.
 struct TablesLayout {
-  size_t w_in;     // [Q*d][D]  f32, the weights as given
   size_t w_in_hi;  // [Q*d][D]  f32, TF32-truncated high part
   size_t w_in_lo;  // [Q*d][D]  f32, w_in - w_in_hi (exact)
   size_t b_in;     // [Q*d]     f32 (zeros when absent)
-  size_t cb;       // [Q][K][d] f32 codebook
-  size_t cbT;      // [Q][d][K] f32 codebook, code-space-major
   size_t cnorm;    // [Q][K]    f32 squared norms (float64 sums)
+  size_t cb_img;   // [Q][K/128][hi,lo][2][128 x 32] f32: -2*codebook split in TF32 hi/lo,
+                   //   each 128-codeword chunk as two 128-byte-swizzled K-major atoms
   size_t z;        // [Q][K][D] f32 decode table
   size_t g;        // [P][K][d] f32 cross-stage table, P = Q(Q-1)/2
   size_t m64;      // [P][d][d] f64 w_in[q] . w_out[s]   (prepare temporary)
@@ -40,13 +42,11 @@ inline TablesLayout tables_layout(const rvq_dims &dm) {
   TablesLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
-  L.w_in = take(Q * d * D * 4);
   L.w_in_hi = take(Q * d * D * 4);
   L.w_in_lo = take(Q * d * D * 4);
   L.b_in = take(Q * d * 4);
-  L.cb = take(Q * K * d * 4);
-  L.cbT = take(Q * d * K * 4);
   L.cnorm = take(Q * K * 4);
+  L.cb_img = take(Q * K * d * 2 * 4);
   L.z = take(Q * K * D * 4);
   L.g = take((P ? P : 1) * K * d * 4);
   L.m64 = take((P ? P : 1) * d * d * 8);
@@ -65,7 +65,7 @@ inline const T *at(const void *base, size_t off) {
 // Launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t s);
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0,
-                                int64_t n, int n_q, int32_t *codes, float *p0, cudaStream_t s);
+                                int64_t n, int n_q, int32_t *codes, float *p0, int *status, cudaStream_t s);
 cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t *codes, int64_t n,
                           int n_q, float *y, int64_t *bad, cudaStream_t s);
 

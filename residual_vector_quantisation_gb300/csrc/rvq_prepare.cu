@@ -14,6 +14,7 @@
 // residual_q = x - sum_{s<q} Z[s][code_s], the stage-q projection is
 // w_in[q] . x + b_in[q] - sum_{s<q} G[q][s][code_s].
 #include "rvq_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace rvq {
 namespace {
@@ -22,38 +23,48 @@ __device__ __forceinline__ float tf32_trunc(float v) {
   return __uint_as_float(__float_as_uint(v) & 0xffffe000u);
 }
 
-// w_in plain / TF32 hi / lo copies and b_in.
-__global__ void k_prep_w_in(const float *__restrict__ w_in, const float *__restrict__ b_in,
-                            float *__restrict__ plain, float *__restrict__ hi, float *__restrict__ lo,
-                            float *__restrict__ b_out_copy, int64_t n, int64_t nb) {
+// w_in TF32 hi / lo split and b_in.
+__global__ void k_prep_w_in(const float *__restrict__ w_in, const float *__restrict__ b_in, float *__restrict__ hi,
+                            float *__restrict__ lo, float *__restrict__ b_in_copy, int64_t n, int64_t nb) {
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t e = i; e < n; e += stride) {
     float v = w_in[e];
     float h = tf32_trunc(v);
-    plain[e] = v;
     hi[e] = h;
     lo[e] = v - h;
   }
-  for (int64_t e = i; e < nb; e += stride) b_out_copy[e] = b_in ? b_in[e] : 0.0f;
+  for (int64_t e = i; e < nb; e += stride) b_in_copy[e] = b_in ? b_in[e] : 0.0f;
 }
 
-// Codebook copy, code-space-major transpose and squared norms.
-__global__ void k_prep_codebook(const float *__restrict__ cb_in, float *__restrict__ cb,
-                                float *__restrict__ cbT, float *__restrict__ cnorm, int K, int d,
-                                int64_t n_rows) {
+// Squared codebook norms (float64 sums).
+__global__ void k_prep_cnorm(const float *__restrict__ cb, float *__restrict__ cnorm, int d, int64_t n_rows) {
   int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // row = q*K + k
   if (r >= n_rows) return;
-  int q = (int)(r / K), k = (int)(r % K);
-  const float *src = cb_in + r * d;
+  const float *src = cb + r * d;
   double s = 0.0;
-  for (int j = 0; j < d; ++j) {
-    float v = src[j];
-    cb[r * d + j] = v;
-    cbT[((int64_t)q * d + j) * K + k] = v;
-    s += (double)v * (double)v;
-  }
+  for (int j = 0; j < d; ++j) s += (double)src[j] * (double)src[j];
   cnorm[r] = (float)s;
+}
+
+// -2 * codebook in TF32 hi/lo halves, laid out as the shared-memory image the
+// tensor-core search loads with one bulk copy per half chunk:
+// [q][chunk of 128][hi, lo][atom j/32][sw128(row = k % 128, j % 32)].
+__global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ img, int K, int64_t n) {
+  constexpr int d = kCodeDim;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*K*d
+  if (e >= n) return;
+  const int j = (int)(e % d);
+  const int64_t qk = e / d;
+  const int q = (int)(qk / K), k = (int)(qk % K);
+  const int c = k / kChunkCodes, kk = k % kChunkCodes;
+  const float v = -2.0f * cb[e];
+  const float hi = tf32_trunc(v);
+  const float lo = v - hi;
+  const int64_t chunk = ((int64_t)q * (K / kChunkCodes) + c) * 2;
+  const uint32_t off = ptx::sw128_offset(kk, j & 31) / 4 + (j >> 5) * (128 * 32);
+  img[(chunk + 0) * (2 * 128 * 32) + off] = hi;
+  img[(chunk + 1) * (2 * 128 * 32) + off] = lo;
 }
 
 // Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64).
@@ -145,13 +156,12 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
   const TablesLayout L = tables_layout(dm);
   const int D = dm.D, d = dm.d, K = dm.K, Q = dm.Q;
   const int64_t nw = (int64_t)Q * d * D, P = n_pairs(Q);
-  k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in), at<float>(tables, L.w_in_hi),
-                                   at<float>(tables, L.w_in_lo), at<float>(tables, L.b_in), nw,
-                                   (int64_t)Q * d);
+  k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
+                                   at<float>(tables, L.b_in), nw, (int64_t)Q * d);
   const int64_t rows = (int64_t)Q * K;
-  k_prep_codebook<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb),
-                                                                  at<float>(tables, L.cbT),
-                                                                  at<float>(tables, L.cnorm), K, d, rows);
+  k_prep_cnorm<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cnorm), d, rows);
+  const int64_t ncb = (int64_t)Q * K * d;
+  k_prep_cb_img<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb);
   k_prep_z<<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
                                                                           at<float>(tables, L.z), D, K);
   if (P > 0) {

@@ -72,7 +72,7 @@ def test_static_scratch_prefix_depth(prepared):
 def test_static_scratch_refuses_calls_that_do_not_fit(prepared):
     rvq, _ = prepared
     row = rvq.Q * rvq.d * 4
-    n_max = rq.RVQ_STATIC_SCRATCH_BYTES // row
+    n_max = (rq.RVQ_STATIC_SCRATCH_BYTES - 256) // row  # a 256-byte status header, then the projections
     big = torch.zeros((n_max + 1, rvq.D), dtype=torch.float32, device=DEV)
     codes = torch.empty((n_max + 1, rvq.Q), dtype=torch.int32, device=DEV)
     with pytest.raises(rq.RVQError) as err:
