@@ -240,63 +240,63 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 
 // ===========================================================================
 // step 2: the stage loop in code space.
-// CTA item: 256 frames as two M=128 tiles that walk the stages in lockstep
-// and share every codebook chunk.  Chunk = 128 codewords; its -2*c hi and lo
-// halves arrive as two 32 KB bulk copies of pre-swizzled images.  Per chunk
-// and tile the accumulator is 128 lanes x 128 columns of TMEM, double
-// buffered so the argmin of chunk c overlaps the MMAs of chunk c+1.
-// Warps: 0 bulk-copy producer, 1 MMA issuer (+ TMEM owner), 2-9 one thread
-// per frame row: build the stage's query p_q, then scan the distances.
+// CTA item: one tile of 128 frames; two CTAs share each SM's tensor core, so
+// one CTA's stage boundaries and distance scans overlap the other's MMAs.
+// The query tile (A operand, hi and lo) lives in TMEM, written by the row
+// threads with tcgen05.st; shared memory holds only a ring of codebook
+// half-chunks: 128 codewords of -2*c, hi or lo, pre-swizzled, 32 KB per bulk
+// copy.  TMEM (256 columns): [0,64) A hi, [64,128) A lo, [128,256) distances.
+// Warps: 0 bulk-copy producer, 1 MMA issuer (+ TMEM owner), 2-5 one thread per
+// frame row: build the stage's query, then scan the distances.
 // ===========================================================================
 constexpr int SR_KC = 128;
 constexpr int SR_STAGES = 3;
-constexpr uint32_t SR_ATOM = 128 * 128;            // 128 rows x 128 B
-constexpr uint32_t SR_A_BYTES = 2 * 2 * 2 * SR_ATOM;  // [tile][hi,lo][atom] = 128 KB
-constexpr uint32_t SR_B_STAGE = 2 * SR_ATOM;          // [atom] = 32 KB
-constexpr int SR_THREADS = 320;
+constexpr uint32_t SR_ATOM = 128 * 128;      // 128 rows x 128 B
+constexpr uint32_t SR_B_STAGE = 2 * SR_ATOM;  // [atom] = 32 KB
+constexpr int SR_THREADS = 192;
+constexpr uint32_t SR_TMEM_COLS = 256;
+constexpr uint32_t SR_A_HI = 0, SR_A_LO = 64, SR_ACC = 128;
 constexpr uint32_t SR_IDESC = idesc_tf32(128, SR_KC);
 
+constexpr int SR_MAX_K = 1024;  // codewords whose norms fit the per-stage smem copy (larger K reads global)
 struct SrBars {
   uint64_t b_full[SR_STAGES], b_empty[SR_STAGES];
-  uint64_t a_ready[2];
-  uint64_t acc_full[2][2];
-  uint64_t acc_empty[2];
-  uint64_t drain;
+  uint64_t a_ready, acc_full, acc_empty, drain;
   uint32_t tmem;
 };
-constexpr size_t SR_SMEM = 1024 + SR_A_BYTES + SR_STAGES * SR_B_STAGE + sizeof(SrBars);
+constexpr size_t SR_CN_BYTES = 2 * SR_MAX_K * 4;  // ||c||^2 of the current stage, double-buffered by stage parity
+constexpr size_t SR_SMEM = 1024 + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + sizeof(SrBars);
 
-__global__ void __launch_bounds__(SR_THREADS, 1)
+__global__ void __launch_bounds__(SR_THREADS, 2)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
                 int n_items, int *__restrict__ status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
-  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_A_BYTES + SR_STAGES * SR_B_STAGE);
+  float *cn_smem = reinterpret_cast<float *>(smem + SR_STAGES * SR_B_STAGE);
+  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkc = K / SR_KC;
+  // Every CTA walks the same codebook chunks; starting each CTA at a different
+  // chunk spreads the simultaneous bulk copies over nkc chunks of L2 instead
+  // of one hot chunk.  The argmin merge below is order-independent.
+  const int rot = blockIdx.x % nkc;
   constexpr int d = kCodeDim;
-  auto a_tile = [&](int t, int hl, int atom) { return smem + ((t * 2 + hl) * 2 + atom) * SR_ATOM; };
-  auto b_stage = [&](int s, int atom) { return smem + SR_A_BYTES + s * SR_B_STAGE + atom * SR_ATOM; };
 
   if (tid == 0) {
     for (int s = 0; s < SR_STAGES; ++s) {
       mbar_init(&bar.b_full[s], 1);
       mbar_init(&bar.b_empty[s], 1);
     }
-    mbar_init(&bar.a_ready[0], 128);
-    mbar_init(&bar.a_ready[1], 128);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar.acc_full[b][0], 1);
-      mbar_init(&bar.acc_full[b][1], 1);
-      mbar_init(&bar.acc_empty[b], 256);
-    }
+    mbar_init(&bar.a_ready, 128);
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.acc_empty, 128);
     mbar_init(&bar.drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bar.tmem, 512);
+    tmem_alloc(&bar.tmem, SR_TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   const uint32_t tmem = bar.tmem;
 
   if (warp == 0) {
-    // ---------------- producer: codebook chunk images ----------------
+    // ---------------- producer: codebook half-chunk images ----------------
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         for (int q = 0; q < n_q && ok; ++q)
           for (int c = 0; c < nkc && ok; ++c)
             for (int h = 0; h < 2; ++h, ++it) {
+              const int cr = (c + rot) % nkc;
               const int s = it % SR_STAGES;
               const uint32_t use = it / SR_STAGES;
               if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
@@ -321,8 +322,8 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
                 break;
               }
               mbar_arrive_expect_tx(&bar.b_full[s], SR_B_STAGE);
-              const float *src = cb_img + ((((size_t)q * nkc + c) * 2 + h) * SR_B_STAGE) / 4;
-              bulk_g2s(b_stage(s, 0), src, SR_B_STAGE, &bar.b_full[s]);
+              const float *src = cb_img + ((((size_t)q * nkc + cr) * 2 + h) * SR_B_STAGE) / 4;
+              bulk_g2s(smem + s * SR_B_STAGE, src, SR_B_STAGE, &bar.b_full[s]);
             }
       for (uint32_t k = 0; k < SR_STAGES && k < it; ++k) {
         const uint32_t j = it - 1 - k;
@@ -341,48 +342,36 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         }
         return ok;
       };
+      // descriptor of the smem base; operand descriptors add (byte offset >> 4)
+      const uint64_t desc0 = smem_desc(smem_addr(smem), 16, 1024, kSwizzle128B);
+      auto dB = [&](int s, int ks) {
+        return desc0 + (uint64_t)((s * SR_B_STAGE + (ks >> 2) * SR_ATOM + (ks & 3) * 32) >> 4);
+      };
+      const uint32_t acc = tmem + SR_ACC;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
         for (int q = 0; q < n_q && ok; ++q, ++builds)
           for (int c = 0; c < nkc && ok; ++c, ++cc) {
-            const int b = cc & 1;
-            const uint32_t use = cc >> 1;
-            if (use > 0 && !wait_or_fail(&bar.acc_empty[b], (use - 1) & 1)) break;
+            if (cc > 0 && !wait_or_fail(&bar.acc_empty, (cc - 1) & 1)) break;
             // hi half: a_hi . b_hi + a_lo . b_hi
             int s = it % SR_STAGES;
             if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
+            if (c == 0 && !wait_or_fail(&bar.a_ready, builds & 1)) break;
             tc_fence_after();
-            for (int t = 0; t < 2; ++t) {
-              if (c == 0 && !wait_or_fail(&bar.a_ready[t], builds & 1)) break;
-              tc_fence_after();
-              const uint32_t dt = tmem + b * 256 + t * SR_KC;
 #pragma unroll
-              for (int ks = 0; ks < d / 8; ++ks) {
-                const uint32_t off = (ks & 3) * 32;
-                const uint64_t ah = smem_desc(smem_addr(a_tile(t, 0, ks >> 2)) + off, 16, 1024, kSwizzle128B);
-                const uint64_t al = smem_desc(smem_addr(a_tile(t, 1, ks >> 2)) + off, 16, 1024, kSwizzle128B);
-                const uint64_t bh = smem_desc(smem_addr(b_stage(s, ks >> 2)) + off, 16, 1024, kSwizzle128B);
-                mma_tf32(dt, ah, bh, SR_IDESC, ks ? 1u : 0u);
-                mma_tf32(dt, al, bh, SR_IDESC, 1u);
-              }
+            for (int ks = 0; ks < d / 8; ++ks) {
+              const uint64_t bh = dB(s, ks);
+              mma_tf32_ta(acc, tmem + SR_A_HI + ks * 8, bh, SR_IDESC, ks ? 1u : 0u);
+              mma_tf32_ta(acc, tmem + SR_A_LO + ks * 8, bh, SR_IDESC, 1u);
             }
-            if (!ok) break;
             mma_commit(&bar.b_empty[s]);
             ++it;
             // lo half: a_hi . b_lo
             s = it % SR_STAGES;
             if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
             tc_fence_after();
-            for (int t = 0; t < 2; ++t) {
-              const uint32_t dt = tmem + b * 256 + t * SR_KC;
 #pragma unroll
-              for (int ks = 0; ks < d / 8; ++ks) {
-                const uint32_t off = (ks & 3) * 32;
-                const uint64_t ah = smem_desc(smem_addr(a_tile(t, 0, ks >> 2)) + off, 16, 1024, kSwizzle128B);
-                const uint64_t bl = smem_desc(smem_addr(b_stage(s, ks >> 2)) + off, 16, 1024, kSwizzle128B);
-                mma_tf32(dt, ah, bl, SR_IDESC, 1u);
-              }
-              mma_commit(&bar.acc_full[b][t]);
-            }
+            for (int ks = 0; ks < d / 8; ++ks) mma_tf32_ta(acc, tmem + SR_A_HI + ks * 8, dB(s, ks), SR_IDESC, 1u);
+            mma_commit(&bar.acc_full);
             mma_commit(&bar.b_empty[s]);
             ++it;
           }
@@ -390,91 +379,120 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       mbar_wait(&bar.drain, 0);
     }
   } else {
-    // ---------------- one thread per frame row (warps 2..9) ----------------
-    const int rt = tid - 64;            // 0..255
-    const int t = rt >> 7;              // tile
+    // ---------------- one thread per frame row (warps 2..5) ----------------
+    // Stage q's query is p_q = P0[n][q] - sum_{s<q} G[q][s][code_s], built
+    // between stages (the co-resident CTA keeps the tensor core busy meanwhile).
     const int quarter = warp & 3;       // TMEM lane quarter of this warp
-    const int r = quarter * 32 + lane;  // row within the tile
-    uint32_t cc = 0;
+    const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+    const int rt = tid - 64;            // 0..127
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int64_t ld = (int64_t)n_q * d;
+    const bool cn_in_smem = K <= SR_MAX_K;
+    uint32_t cc = 0, stage_count = 0;
     bool ok = true;
+    int my_codes[kMaxStages];
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int64_t n = (int64_t)item * 256 + t * 128 + r;
+      const int64_t n = (int64_t)item * 128 + r;
       const bool valid = n < n_rows;
-      int32_t *crow = codes + (valid ? n : 0) * n_q;
-      for (int q = 0; q < n_q && ok; ++q) {
-        // ---- query p_q = P0[n][q] - sum_{s<q} G[q][s][code_s]
-        float p[d];
-        if (valid) {
-          const float4 *src = reinterpret_cast<const float4 *>(P0 + n * (int64_t)(n_q * d) + q * d);
+      for (int q = 0; q < n_q && ok; ++q, ++stage_count) {
+        // ---- query p_q
+        {
+          float p[d];
+          if (valid) {
+            const float4 *src = reinterpret_cast<const float4 *>(P0 + n * ld + q * d);
 #pragma unroll
-          for (int u = 0; u < d / 4; ++u) *reinterpret_cast<float4 *>(&p[4 * u]) = src[u];
-          for (int s = 0; s < q; ++s) {
-            const float4 *g = reinterpret_cast<const float4 *>(G + (pair_index(q, s) * K + crow[s]) * d);
+            for (int u = 0; u < d / 4; ++u) *reinterpret_cast<float4 *>(&p[4 * u]) = src[u];
+            for (int s = 0; s < q; ++s) {
+              const float4 *g = reinterpret_cast<const float4 *>(G + (pair_index(q, s) * K + my_codes[s]) * d);
 #pragma unroll
-            for (int u = 0; u < d / 4; ++u) {
-              const float4 v = __ldg(g + u);
-              p[4 * u] -= v.x;
-              p[4 * u + 1] -= v.y;
-              p[4 * u + 2] -= v.z;
-              p[4 * u + 3] -= v.w;
+              for (int u = 0; u < d / 4; ++u) {
+                const float4 v = __ldg(g + u);
+                p[4 * u] -= v.x;
+                p[4 * u + 1] -= v.y;
+                p[4 * u + 2] -= v.z;
+                p[4 * u + 3] -= v.w;
+              }
             }
+          } else {
+#pragma unroll
+            for (int u = 0; u < d; ++u) p[u] = 0.f;
           }
-        } else {
+          // A operand: raw (= hi after TF32 truncation) and lo parts into this row's TMEM lane
 #pragma unroll
-          for (int u = 0; u < d; ++u) p[u] = 0.f;
-        }
-        // raw (= hi after TF32 truncation) and lo rows, 128-byte swizzled K-major
+          for (int h = 0; h < 2; ++h) {
+            float lo[32];
 #pragma unroll
-        for (int u = 0; u < d / 4; ++u) {
-          const int j = 4 * u;
-          const uint32_t off = sw128_offset(r, j & 31);
-          float4 h = make_float4(p[j], p[j + 1], p[j + 2], p[j + 3]);
-          float4 l;
-          l.x = h.x - __uint_as_float(__float_as_uint(h.x) & 0xffffe000u);
-          l.y = h.y - __uint_as_float(__float_as_uint(h.y) & 0xffffe000u);
-          l.z = h.z - __uint_as_float(__float_as_uint(h.z) & 0xffffe000u);
-          l.w = h.w - __uint_as_float(__float_as_uint(h.w) & 0xffffe000u);
-          *reinterpret_cast<float4 *>(a_tile(t, 0, j >> 5) + off) = h;
-          *reinterpret_cast<float4 *>(a_tile(t, 1, j >> 5) + off) = l;
+            for (int i = 0; i < 32; ++i) {
+              const float v = p[32 * h + i];
+              lo[i] = v - __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+            }
+            tmem_st32(lane_base + SR_A_HI + 32 * h, *reinterpret_cast<const float(*)[32]>(&p[32 * h]));
+            tmem_st32(lane_base + SR_A_LO + 32 * h, lo);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar.a_ready);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar.a_ready[t]);
-        // ---- scan the K distances ||c||^2 - 2 p.c in ascending k
+        // ---- this stage's squared norms into smem (the previous use of this buffer
+        //      ended before every row thread passed the previous stage's barrier)
+        const float *cnq = cnorm + (int64_t)q * K;
+        float *cns = cn_smem + (stage_count & 1) * SR_MAX_K;
+        if (cn_in_smem) {
+          for (int e = rt * 4; e < K; e += 128 * 4)
+            *reinterpret_cast<float4 *>(cns + e) = __ldg(reinterpret_cast<const float4 *>(cnq + e));
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        const float *cnsrc = cn_in_smem ? cns : cnq;
+        // ---- scan the K distances ||c||^2 - 2 p.c; keep the lexicographic (value, index) minimum
         float best_v = __int_as_float(0x7f800000);
         int best_k = 0;
-        const float *cnq = cnorm + (int64_t)q * K;
         for (int c = 0; c < nkc; ++c, ++cc) {
-          const int b = cc & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full[b][t], (cc >> 1) & 1))) {
+          const int cr = (c + rot) % nkc;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full, cc & 1))) {
             record_error(status, RVQ_DEVICE_TIMEOUT);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + b * 256 + t * SR_KC;
+          float v[SR_KC];
 #pragma unroll
-          for (int g = 0; g < SR_KC / 32; ++g) {
-            float v[32];
-            tmem_ld32(ta + g * 32, v);
-            tmem_wait_ld();
-            const float4 *cn4 = reinterpret_cast<const float4 *>(cnq + c * SR_KC + g * 32);
+          for (int g = 0; g < SR_KC / 32; ++g)
+            tmem_ld32(lane_base + SR_ACC + g * 32, *reinterpret_cast<float(*)[32]>(&v[32 * g]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar.acc_empty);  // the accumulator is free: the values are in registers
+          const float4 *cn4 = reinterpret_cast<const float4 *>(cnsrc + cr * SR_KC);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float4 cn = __ldg(cn4 + u);
-              const float e[4] = {v[4 * u] + cn.x, v[4 * u + 1] + cn.y, v[4 * u + 2] + cn.z, v[4 * u + 3] + cn.w};
+          for (int u = 0; u < SR_KC / 4; ++u) {
+            const float4 cn = cn4[u];
+            v[4 * u] += cn.x;
+            v[4 * u + 1] += cn.y;
+            v[4 * u + 2] += cn.z;
+            v[4 * u + 3] += cn.w;
+          }
+          float mm[SR_KC / 2];
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (e[i] < best_v) {
-                  best_v = e[i];
-                  best_k = c * SR_KC + g * 32 + 4 * u + i;
-                }
+          for (int i = 0; i < SR_KC / 2; ++i) mm[i] = fminf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+          for (int w2 = SR_KC / 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+            for (int i = 0; i < w2; ++i) mm[i] = fminf(mm[i], mm[i + w2]);
+          const float m = mm[0];
+          if (m <= best_v) {  // rare after the first chunks: locate the first index holding m
+            int first = SR_KC - 1;
+#pragma unroll
+            for (int i = SR_KC - 1; i >= 0; --i)
+              if (v[i] == m) first = i;
+            const int k = cr * SR_KC + first;
+            if (m < best_v || k < best_k) {
+              best_v = m;
+              best_k = k;
             }
           }
-          tc_fence_before();
-          mbar_arrive(&bar.acc_empty[b]);
         }
         if (!ok) break;
-        if (valid) crow[q] = best_k;
+        my_codes[q] = best_k;
+        if (valid) codes[n * n_q + q] = best_k;
       }
     }
   }
@@ -482,7 +500,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, SR_TMEM_COLS);
   }
 }
 
@@ -566,9 +584,10 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   k_project_tc<<<items1 < sms ? items1 : sms, PJ_THREADS, PJ_SMEM, st>>>(
       tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_search_tc<<<n_pairs_rows < sms ? n_pairs_rows : sms, SR_THREADS, SR_SMEM, st>>>(
+  const int tiles = (int)((n + 127) / 128);
+  k_search_tc<<<tiles < 2 * sms ? tiles : 2 * sms, SR_THREADS, SR_SMEM, st>>>(
       p0, at<float>(tables, L.g), at<float>(tables, L.cb_img), at<float>(tables, L.cnorm), codes + n0 * n_q, n, n_q,
-      K, n_pairs_rows, status);
+      K, tiles, status);
   return cudaGetLastError();
 }
 
