@@ -433,6 +433,12 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
           tc_fence_before();
           mbar_arrive(&bar.a_ready);
         }
+        // the next stage's projections do not depend on this stage's code: pull them into L2 now
+        if (valid && q + 1 < n_q) {
+          const float *nxt = P0 + n * ld + (q + 1) * d;
+          prefetch_l2(nxt);
+          prefetch_l2(nxt + 32);
+        }
         // ---- this stage's squared norms into smem (the previous use of this buffer
         //      ended before every row thread passed the previous stage's barrier)
         const float *cnq = cnorm + (int64_t)q * K;
