@@ -161,6 +161,36 @@ RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const floa
                                    int64_t n_frames, int32_t n_q, int32_t *codes, float *x_hat,
                                    void *scratch, size_t scratch_bytes, rvq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Host-memory pipeline: frames in host memory in, codes and reconstruction in
+ * host memory out.  The frames are processed in chunks of chunk_frames
+ * through three device buffer slots carved from a caller-owned workspace;
+ * three streams overlap the host-to-device copy of one chunk, the encode +
+ * decode of the previous one and the device-to-host copy of the one before
+ * (pinned host memory lets the copies run at full speed).  The pipeline owns
+ * three CUDA streams and nine events on the device that was current at
+ * creation; it allocates no memory.  One pipeline serves one call at a time.
+ * --------------------------------------------------------------------------- */
+typedef struct rvq_pipeline rvq_pipeline;
+
+/* Workspace bytes for a pipeline (0 for unsupported arguments). */
+RVQ_API size_t rvq_pipeline_workspace_bytes(rvq_dims dims, int32_t n_q, int64_t chunk_frames);
+
+/* Create a pipeline for depth n_q over `workspace` (device memory, 256-byte
+ * aligned, at least rvq_pipeline_workspace_bytes, caller-owned and reserved
+ * until rvq_pipeline_destroy).  *out receives the pipeline. */
+RVQ_API rvq_status rvq_pipeline_create(rvq_dims dims, int32_t n_q, int64_t chunk_frames, void *workspace,
+                                       size_t workspace_bytes, rvq_pipeline **out);
+
+/* Wait for the pipeline's work, release its streams and events, free it. */
+RVQ_API rvq_status rvq_pipeline_destroy(rvq_pipeline *pipeline);
+
+/* Encode and decode n_frames host frames x_host [N][D] with the tables of
+ * rvq_prepare: codes_host [N][n_q] (required) and x_hat_host [N][D]
+ * (nullable).  Synchronous: returns when every output is in host memory. */
+RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *pipeline, const void *tables, const float *x_host,
+                                            int64_t n_frames, int32_t *codes_host, float *x_hat_host);
+
 /* Encode like rvq_encode, but with no scratch argument: for callers that
  * cannot allocate device memory when they encode (a real-time audio callback,
  * where cudaMalloc may stall on device-wide synchronisation, or an application

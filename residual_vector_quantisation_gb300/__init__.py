@@ -29,7 +29,8 @@ __all__ = [
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "RVQ_STATIC_SCRATCH_BYTES", "RVQ",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "rvq_pipeline_workspace_bytes", "rvq_pipeline_create", "rvq_pipeline_destroy",
+    "rvq_pipeline_reconstruct", "RVQPipeline",
 ]
 
 RVQ_OK = 0
@@ -39,7 +40,8 @@ STATUS_NAMES = {0: "RVQ_OK", -1: "RVQ_ERR_INVALID_ARG", -2: "RVQ_ERR_UNSUPPORTED
 EXPORTED_SYMBOLS = [
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
-    "rvq_status_string", "rvq_version", "rvq_encode_static",
+    "rvq_status_string", "rvq_version", "rvq_encode_static", "rvq_pipeline_workspace_bytes",
+    "rvq_pipeline_create", "rvq_pipeline_destroy", "rvq_pipeline_reconstruct",
 ]
 
 RVQ_STATIC_SCRATCH_BYTES = 16 << 20  # include/rvq.h
@@ -90,6 +92,10 @@ def load_library(path: Optional[str] = None):
         "rvq_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "rvq_version": ([], ctypes.c_char_p),
         "rvq_encode_static": ([rvq_dims, vp, vp, i64, i32, vp, vp], ctypes.c_int),
+        "rvq_pipeline_workspace_bytes": ([rvq_dims, i32, i64], sz),
+        "rvq_pipeline_create": ([rvq_dims, i32, i64, vp, sz, ctypes.POINTER(vp)], ctypes.c_int),
+        "rvq_pipeline_destroy": ([vp], ctypes.c_int),
+        "rvq_pipeline_reconstruct": ([vp, vp, vp, i64, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -179,6 +185,35 @@ def rvq_encode_static(dims: rvq_dims, tables, x, n_q: int, codes, stream=None) -
                                                                  _ptr(codes), _stream(stream)))
 
 
+def rvq_pipeline_workspace_bytes(dims: rvq_dims, n_q: int, chunk_frames: int) -> int:
+    return load_library().rvq_pipeline_workspace_bytes(dims, int(n_q), int(chunk_frames))
+
+
+def rvq_pipeline_create(dims: rvq_dims, n_q: int, chunk_frames: int, workspace: torch.Tensor) -> ctypes.c_void_p:
+    out = ctypes.c_void_p()
+    _check("rvq_pipeline_create", load_library().rvq_pipeline_create(
+        dims, int(n_q), int(chunk_frames), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(out)))
+    return out
+
+
+def rvq_pipeline_destroy(pipeline) -> None:
+    _check("rvq_pipeline_destroy", load_library().rvq_pipeline_destroy(pipeline))
+
+
+def _host_ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("host buffers must be contiguous CPU tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def rvq_pipeline_reconstruct(pipeline, tables, x_host, codes_host, x_hat_host=None) -> None:
+    _check("rvq_pipeline_reconstruct", load_library().rvq_pipeline_reconstruct(
+        pipeline, _ptr(tables), _host_ptr(x_host), x_host.shape[0], _host_ptr(codes_host), _host_ptr(x_hat_host)))
+
+
 def rvq_status_string(status: int) -> str:
     return load_library().rvq_status_string(int(status)).decode()
 
@@ -252,3 +287,43 @@ class RVQ:
             x_hat = torch.empty((n, self.D), dtype=torch.float32, device=self.device)
         rvq_reconstruct(self.dims, self.tables, x, n_q, codes, x_hat, self.scratch_for(n, n_q), stream)
         return codes, x_hat
+
+
+class RVQPipeline:
+    """Encode + decode of frames held in host memory, copies overlapped with compute.
+
+    Wraps rvq_pipeline_*: the device workspace is a torch allocation owned by
+    this object.  Pinned host tensors give full copy bandwidth.
+    """
+
+    def __init__(self, rvq: "RVQ", n_q: Optional[int] = None, chunk_frames: int = 38912):
+        self.rvq = rvq
+        self.n_q = rvq.Q if n_q is None else int(n_q)
+        nbytes = rvq_pipeline_workspace_bytes(rvq.dims, self.n_q, chunk_frames)
+        if nbytes == 0:
+            raise ValueError("unsupported pipeline arguments")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=rvq.device)
+        with torch.cuda.device(rvq.device):
+            self.handle = rvq_pipeline_create(rvq.dims, self.n_q, chunk_frames, self.workspace)
+
+    def reconstruct(self, x_host: torch.Tensor, codes_host: Optional[torch.Tensor] = None,
+                    x_hat_host: Optional[torch.Tensor] = None, want_x_hat: bool = True):
+        n = x_host.shape[0]
+        if codes_host is None:
+            codes_host = torch.empty((n, self.n_q), dtype=torch.int32, pin_memory=True)
+        if x_hat_host is None and want_x_hat:
+            x_hat_host = torch.empty((n, self.rvq.D), dtype=torch.float32, pin_memory=True)
+        with torch.cuda.device(self.rvq.device):
+            rvq_pipeline_reconstruct(self.handle, self.rvq.tables, x_host, codes_host, x_hat_host)
+        return codes_host, x_hat_host
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            rvq_pipeline_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -40,6 +40,11 @@ int main(void) {
   EXPECT(rvq_decode(ok, NULL, fake_codes, 1, 8, NULL, NULL, NULL) == RVQ_ERR_INVALID_ARG);
   EXPECT(rvq_decode(ok, NULL, NULL, 1, 9, NULL, NULL, NULL) == RVQ_ERR_INVALID_ARG);
   EXPECT(rvq_reconstruct(bad_d, NULL, NULL, 1, 8, NULL, NULL, NULL, 0, NULL) == RVQ_ERR_UNSUPPORTED);
+  EXPECT(rvq_pipeline_workspace_bytes(ok, 8, 1024) > 0);
+  EXPECT(rvq_pipeline_workspace_bytes(ok, 9, 1024) == 0);
+  EXPECT(rvq_pipeline_create(ok, 8, 1024, NULL, 0, NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_pipeline_destroy(NULL) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_pipeline_reconstruct(NULL, NULL, NULL, 1, NULL, NULL) == RVQ_ERR_INVALID_ARG);
   EXPECT(strcmp(rvq_status_string(RVQ_OK), "ok") == 0);
   EXPECT(rvq_status_string(RVQ_ERR_CUDA) != NULL);
   EXPECT(rvq_version() != NULL && strlen(rvq_version()) > 0);

@@ -1,0 +1,53 @@
+"""The host-memory pipeline (rvq_pipeline_*): frames in pinned host memory go
+through chunked copies overlapped with encode + decode; the results must be
+identical to the device-buffer entry points on the same frames."""
+
+import numpy as np
+import pytest
+import torch
+
+import rvq_inputs as ri
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import residual_vector_quantisation_gb300 as rq  # noqa: E402
+from residual_vector_quantisation_gb300 import build as rqb  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def rvq():
+    rqb.build_library()
+    rq.load_library()
+    w = ri.WORKLOAD_BY_NAME["tiny"]
+    W = ri.weights_to_torch(ri.make_weights(w, with_bias=True), DEV)
+    return rq.RVQ(W["w_in"], W["codebook"], W["w_out"], W["b_in"], W["b_out"], device=DEV)
+
+
+@pytest.mark.parametrize("n,chunk,n_q", [(250, 100, 8), (1000, 128, 8), (77, 256, 3), (4097, 640, 5)])
+def test_pipeline_matches_device_path(rvq, n, chunk, n_q):
+    x = torch.from_numpy(np.random.default_rng(n).standard_normal((n, rvq.D)).astype(np.float32))
+    x_host = x.pin_memory()
+    pipe = rq.RVQPipeline(rvq, n_q=n_q, chunk_frames=chunk)
+    codes_h, x_hat_h = pipe.reconstruct(x_host)
+    codes_d, x_hat_d = rvq.reconstruct(x.to(DEV), n_q=n_q)
+    torch.cuda.synchronize()
+    assert torch.equal(codes_h, codes_d.cpu())
+    assert torch.equal(x_hat_h, x_hat_d.cpu())
+    # codes only, and a second call on the same pipeline
+    codes2, none = pipe.reconstruct(x_host, want_x_hat=False)
+    assert none is None and torch.equal(codes2, codes_h)
+    pipe.close()
+
+
+def test_pipeline_rejects_bad_arguments(rvq):
+    with pytest.raises(ValueError):
+        rq.RVQPipeline(rvq, n_q=rvq.Q + 1)
+    pipe = rq.RVQPipeline(rvq, chunk_frames=64)
+    with pytest.raises(ValueError):
+        pipe.reconstruct(torch.zeros((4, rvq.D), device=DEV))  # device tensor is not a host buffer
+    pipe.close()
