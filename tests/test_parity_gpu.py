@@ -161,7 +161,8 @@ def test_ragged_frame_counts(N):
     run_small(W, x, label=f"N={N}")
 
 
-@pytest.mark.parametrize("D,K,Q", [(16, 128, 1), (48, 128, 2), (256, 384, 5), (2048, 256, 2)])
+@pytest.mark.parametrize("D,K,Q", [(16, 128, 1), (48, 128, 2), (256, 384, 5), (2048, 256, 2),
+                                   (64, 1152, 2), (96, 256, 20)])
 def test_other_shapes(D, K, Q):
     w, W = _small_weights(D=D, K=K, Q=Q, seed=D + K + Q)
     x = np.random.default_rng(D).standard_normal((300, D)).astype(np.float32)
