@@ -171,6 +171,7 @@ def cpu_baseline_leg(W, x_sample: np.ndarray, w) -> dict:
 def run_ours(args):
     import torch
     import residual_vector_quantisation_gb300 as rq
+    from residual_vector_quantisation_gb300.shard import reduce_max
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -222,11 +223,7 @@ def run_ours(args):
             ev[i][2].record(stream)
         stop.record(stream)
         barrier()
-    ms_total = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(start.elapsed_time(stop), dev)
     ms_step = ms_total / args.steps
     enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
@@ -247,6 +244,7 @@ def e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev):
     copies with encode + decode).  Host wall clock around the synchronous call."""
     import torch
     import residual_vector_quantisation_gb300 as rq
+    from residual_vector_quantisation_gb300.shard import reduce_max
     x_host = x.cpu().pin_memory()
     codes_host = torch.empty(codes.shape, dtype=codes.dtype, pin_memory=True)
     y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
@@ -264,11 +262,7 @@ def e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
     pipe.close()
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return e2e_ms
+    return reduce_max(e2e_ms, dev)
 
 
 def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, clocks, world):

@@ -11,7 +11,6 @@ namespace rvq {
 
 constexpr int kCodeDim = 64;            // d supported by the kernels
 constexpr int kChunkCodes = 128;        // codewords per tensor-core distance chunk
-constexpr int kDecodeSlice = 16;        // output columns per decode slice
 constexpr size_t kScratchHeader = 256;  // status word at the head of encode scratch
 constexpr int RVQ_DEVICE_TIMEOUT = 5;   // status word value: a bounded device wait gave up
 constexpr int kMaxStages = 64;         // Q limit
@@ -31,7 +30,7 @@ struct TablesLayout {
   size_t cnorm;    // [Q][K]    f32 squared norms (float64 sums)
   size_t cb_img;   // [Q][K/128][hi,lo][2][128 x 32] f32: -2*codebook split in TF32 hi/lo,
                    //   each 128-codeword chunk as two 128-byte-swizzled K-major atoms
-  size_t z;        // [D/16][Q][K][16] f32 decode table, slice-major
+  size_t z;        // [Q][K][D] f32 decode table
   size_t g;        // [P][K][d] f32 cross-stage table, P = Q(Q-1)/2
   size_t m64;      // [P][d][d] f64 w_in[q] . w_out[s]   (prepare temporary)
   size_t vb64;     // [P][d]    f64 w_in[q] . b_out[s]   (prepare temporary)

@@ -5,8 +5,7 @@
 // to float64 summation error (about 1e-16 relative).
 //
 //   cnorm[q][k]   = ||codebook[q][k]||^2
-//   Z[q][k]       = w_out[q] . codebook[q][k] + b_out[q]         (decode table,
-//                   stored slice-major: Zs[i / 16][q][k][i % 16])
+//   Z[q][k]       = w_out[q] . codebook[q][k] + b_out[q]         (decode table)
 //   G[q][s][k]    = w_in[q] . Z[s][k]            for s < q      (cross-stage table)
 //
 // Z re-associates the decode graph of omnivoice.cpp ARCHITECTURE.md ("RVQ
@@ -73,7 +72,7 @@ __global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ 
 __global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
                                                 const float *__restrict__ b_out,
                                                 const float *__restrict__ cb, float *__restrict__ z,
-                                                int D, int K, int Q) {
+                                                int D, int K) {
   constexpr int d = kCodeDim;
   __shared__ double sc[16][d];
   const int64_t row0 = (int64_t)blockIdx.y * 16;  // q*K + k0
@@ -92,10 +91,7 @@ __global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
     double s = 0.0;
 #pragma unroll
     for (int j = 0; j < d; ++j) s += w[j] * sc[kk][j];
-    // slice-major: Zs[i / 16][q][k][i % 16]
-    const int64_t k = row0 + kk - (int64_t)q * K;
-    z[((((int64_t)(i / kDecodeSlice) * Q + q) * K + k) * kDecodeSlice) + i % kDecodeSlice] =
-        (float)(s + bias);
+    z[(row0 + kk) * D + i] = (float)(s + bias);
   }
 }
 
@@ -167,7 +163,7 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
   const int64_t ncb = (int64_t)Q * K * d;
   k_prep_cb_img<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb);
   k_prep_z<<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
-                                                                          at<float>(tables, L.z), D, K, Q);
+                                                                          at<float>(tables, L.z), D, K);
   if (P > 0) {
     k_prep_m<<<dim3((unsigned)P, d), d + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
                                                       at<double>(tables, L.vb64), D, Q);

@@ -12,8 +12,12 @@ namespace rvq {
 namespace ptx {
 
 // Polls before a bounded wait gives up (each poll is a try_wait with the
-// hardware's own suspend time hint, so this is far longer than any healthy wait).
-constexpr uint32_t kSpinLimit = 1u << 24;
+// hardware's own suspend time hint, so this is far longer than any healthy
+// wait).  A build may lower it (the bounded-wait self-test does).
+#ifndef RVQ_SPIN_LIMIT
+#define RVQ_SPIN_LIMIT (1u << 24)
+#endif
+constexpr uint32_t kSpinLimit = RVQ_SPIN_LIMIT;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

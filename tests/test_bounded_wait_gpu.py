@@ -1,0 +1,45 @@
+"""A device wait that runs out reports a status instead of hanging.
+
+Every mbarrier wait in the library is bounded (rvq::ptx::mbar_wait).  This
+test builds a kernel, with a short poll limit, that waits on a barrier nothing
+ever arrives at, and checks that it gives up, sets the timeout status (5),
+returns, and that the next kernel on the same context runs normally.  No GPU
+fault or hang is involved."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from residual_vector_quantisation_gb300 import build as rqb  # noqa: E402
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_bounded_wait_times_out_and_context_survives(tmp_path):
+    so = tmp_path / "libselftest.so"
+    subprocess.run([rqb.nvcc(), *rqb.ARCH, "-O2", "-std=c++17", "-DRVQ_SPIN_LIMIT=4096u", "-Xcompiler", "-fPIC",
+                    "-shared", "-I", rqb.CSRC, os.path.join(HERE, "gpu_selftest", "bounded_wait.cu"), "-o", str(so)],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    lib.selftest_bounded_wait.argtypes = [ctypes.c_void_p] * 3
+    lib.selftest_bounded_wait.restype = ctypes.c_int
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    clk = torch.zeros(1, dtype=torch.int64, device="cuda")
+    after = torch.zeros(32, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    rc = lib.selftest_bounded_wait(ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(clk.data_ptr()),
+                                   ctypes.c_void_p(after.data_ptr()))
+    assert rc == 0
+    assert int(status.item()) == 5
+    assert int(clk.item()) > 0
+    assert torch.equal(after.cpu(), torch.arange(1000, 1032, dtype=torch.int32))
+    # and torch's own kernels still run on this context
+    assert float((torch.ones(1024, device="cuda") * 2).sum().item()) == 2048.0
