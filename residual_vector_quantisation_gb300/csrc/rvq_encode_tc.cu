@@ -264,8 +264,10 @@ struct SrBars {
   uint64_t a_ready, acc_full, acc_empty, drain;
   uint32_t tmem;
 };
-constexpr size_t SR_CN_BYTES = 2 * SR_MAX_K * 4;  // ||c||^2 of the current stage, double-buffered by stage parity
-constexpr size_t SR_SMEM = 1024 + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + sizeof(SrBars);
+constexpr size_t SR_CN_BYTES = SR_MAX_K * 4;        // ||c||^2 of the current stage
+constexpr int SR_XPOSE_LD = 20;                       // floats per row of a warp's transpose scratch (16 + pad)
+constexpr size_t SR_XPOSE_BYTES = 4 * 32 * SR_XPOSE_LD * 4;  // 4 row warps x 32 frames
+constexpr size_t SR_SMEM = 1024 + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + SR_XPOSE_BYTES + sizeof(SrBars);
 
 __global__ void __launch_bounds__(SR_THREADS, 2)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
@@ -275,7 +277,8 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
   float *cn_smem = reinterpret_cast<float *>(smem + SR_STAGES * SR_B_STAGE);
-  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES);
+  float *xpose = reinterpret_cast<float *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES);
+  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + SR_XPOSE_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkc = K / SR_KC;
   // Every CTA walks the same codebook chunks; starting each CTA at a different
@@ -395,25 +398,51 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
       const int64_t n = (int64_t)item * 128 + r;
       const bool valid = n < n_rows;
       for (int q = 0; q < n_q && ok; ++q, ++stage_count) {
-        // ---- query p_q
+        // ---- query p_q = P0[n][q] - sum_{s<q} G[q][s][code_s], rows read cooperatively:
+        //      four lanes read 64 contiguous bytes of one frame's row (8 rows per warp
+        //      instruction), and a per-warp shared-memory transpose hands every lane
+        //      its own frame's 64 values.  Terms are added in the same order as a
+        //      plain per-thread sum.
         {
           float p[d];
-          if (valid) {
-            const float4 *src = reinterpret_cast<const float4 *>(P0 + n * ld + q * d);
 #pragma unroll
-            for (int u = 0; u < d / 4; ++u) *reinterpret_cast<float4 *>(&p[4 * u]) = src[u];
-            for (int s = 0; s < q; ++s) {
-              const float4 *g = reinterpret_cast<const float4 *>(G + (pair_index(q, s) * K + my_codes[s]) * d);
+          for (int u = 0; u < d; ++u) p[u] = 0.f;
+          float *xs = xpose + (warp - 2) * 32 * SR_XPOSE_LD;
+          auto coop_accumulate = [&](const float *row, bool add) {
+            const unsigned long long mine = reinterpret_cast<unsigned long long>(row);
 #pragma unroll
-              for (int u = 0; u < d / 4; ++u) {
-                const float4 v = __ldg(g + u);
-                p[4 * u] -= v.x;
-                p[4 * u + 1] -= v.y;
-                p[4 * u + 2] -= v.z;
-                p[4 * u + 3] -= v.w;
+            for (int b = 0; b < d / 16; ++b) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int f = (lane >> 2) + 8 * i, j = lane & 3;
+                const float *src = reinterpret_cast<const float *>(__shfl_sync(0xffffffffu, mine, f));
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(src + 16 * b + 4 * j));
+                *reinterpret_cast<float4 *>(xs + f * SR_XPOSE_LD + 4 * j) = v;
               }
+              __syncwarp();
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float4 v = *reinterpret_cast<const float4 *>(xs + lane * SR_XPOSE_LD + 4 * u);
+                if (add) {
+                  p[16 * b + 4 * u] += v.x;
+                  p[16 * b + 4 * u + 1] += v.y;
+                  p[16 * b + 4 * u + 2] += v.z;
+                  p[16 * b + 4 * u + 3] += v.w;
+                } else {
+                  p[16 * b + 4 * u] -= v.x;
+                  p[16 * b + 4 * u + 1] -= v.y;
+                  p[16 * b + 4 * u + 2] -= v.z;
+                  p[16 * b + 4 * u + 3] -= v.w;
+                }
+              }
+              __syncwarp();
             }
-          } else {
+          };
+          // invalid frames read a valid row and discard the result
+          coop_accumulate(P0 + (valid ? n : 0) * ld + q * d, true);
+          for (int s = 0; s < q; ++s)
+            coop_accumulate(G + (pair_index(q, s) * K + (valid ? my_codes[s] : 0)) * d, false);
+          if (!valid) {
 #pragma unroll
             for (int u = 0; u < d; ++u) p[u] = 0.f;
           }
@@ -439,11 +468,12 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
           prefetch_l2(nxt);
           prefetch_l2(nxt + 32);
         }
-        // ---- this stage's squared norms into smem (the previous use of this buffer
-        //      ended before every row thread passed the previous stage's barrier)
+        // ---- this stage's squared norms into smem, between two barriers of the row
+        //      threads (every row thread has finished the previous stage's scan)
         const float *cnq = cnorm + (int64_t)q * K;
-        float *cns = cn_smem + (stage_count & 1) * SR_MAX_K;
+        float *cns = cn_smem;
         if (cn_in_smem) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
           for (int e = rt * 4; e < K; e += 128 * 4)
             *reinterpret_cast<float4 *>(cns + e) = __ldg(reinterpret_cast<const float4 *>(cnq + e));
           asm volatile("bar.sync 1, 128;" ::: "memory");

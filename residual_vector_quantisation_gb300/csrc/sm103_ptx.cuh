@@ -62,6 +62,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return false;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Latency-critical wait: poll without suspending (test_wait) for a while,
+// then fall back to the suspending bounded wait.  false on timeout.
+__device__ __forceinline__ bool mbar_wait_hot(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (kSpinLimit < 65536u ? kSpinLimit : 65536u); ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity);
+}
+
 // ---------------------------------------------------------------------------
 // proxies and TMA
 // ---------------------------------------------------------------------------
