@@ -380,6 +380,70 @@ def measure_peaks():
     print(json.dumps(out), flush=True)
 
 
+def per_workload_table(args):
+    """Encode and decode throughput for each workload (CUDA events, inputs
+    resident), with its roofline fractions and an oracle sample on the host."""
+    import torch
+    import oracle
+    import residual_vector_quantisation_gb300 as rq
+    dev = torch.device("cuda", 0)
+    peaks = _peaks()
+    tc_peak = peaks["bf16_tflops"] * (1.1 / 2.25) / 3.0
+    rows = []
+    for w in ri.WORKLOADS:
+        W = ri.make_weights(w)
+        Wt = ri.weights_to_torch(W, dev)
+        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], device=dev)
+        n_q = w.Q
+        row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q}
+        if w.kind == "decode":
+            codes = torch.from_numpy(ri.make_codes(w)).to(dev)
+            x_host = None
+        else:
+            x = ri.make_x_torch(w, Wt, dev) if w.N > 20000 else torch.from_numpy(ri.make_x(w, W)).to(dev)
+            codes = torch.empty((w.N, n_q), dtype=torch.int32, device=dev)
+            scratch = rvq.scratch_for(w.N, n_q)
+        y = torch.empty((w.N, w.D), dtype=torch.float32, device=dev)
+
+        def timed(fn, reps=10):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        if w.kind != "decode":
+            enc_ms = timed(lambda: rq.rvq_encode(rvq.dims, rvq.tables, x, n_q, codes, scratch))
+            row["encode_ms"] = enc_ms
+            row["encode_fps"] = w.N / (enc_ms / 1e3)
+            row["encode_frac"] = encode_flops_per_frame(w) * w.N / (enc_ms / 1e3) / 1e12 / tc_peak
+        dec_ms = timed(lambda: rq.rvq_decode(rvq.dims, rvq.tables, codes, n_q, y))
+        row["decode_ms"] = dec_ms
+        row["decode_fps"] = w.N / (dec_ms / 1e3)
+        row["decode_frac_hbm"] = decode_bytes_per_frame(w) * w.N / (dec_ms / 1e3) / 1e9 / peaks["hbm_gbs"]
+        # oracle on the host cores: a bounded sample of the same workload
+        sample = min(w.N, 4096)
+        cores = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        if w.kind == "decode":
+            oracle.decode(W, ri.make_codes(w, np.arange(sample)), threads=cores)
+        else:
+            xs = x[:sample].cpu().numpy()
+            enc = oracle.encode(W, xs, want_residual=False, threads=cores)
+            oracle.decode(W, enc["codes"], threads=cores)
+        row["oracle_fps"] = sample / (time.perf_counter() - t0)
+        row["oracle_cores"] = cores
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del rvq
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,14 +454,17 @@ def main():
     ap.add_argument("--ref-frames", type=int, default=8192, help="oracle frames per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-chunk", type=int, default=38912, help="frames per chunk of the host pipeline")
+    ap.add_argument("--e2e-chunk", type=int, default=19456, help="frames per chunk of the host pipeline")
     ap.add_argument("--workload", default=WORKLOAD, choices=[w.name for w in ri.WORKLOADS])
     ap.add_argument("--frames", type=int, default=0, help="use only the first N frames (profiling)")
     ap.add_argument("--peaks", action="store_true", help="measure TF32/FP32 GEMM and L2 bandwidths instead")
+    ap.add_argument("--table", action="store_true", help="per-workload encode/decode throughput instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
     if args.peaks:
         measure_peaks()
+    elif args.table:
+        per_workload_table(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
