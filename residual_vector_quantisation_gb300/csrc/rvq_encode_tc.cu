@@ -410,15 +410,21 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
           float *xs = xpose + (warp - 2) * 32 * SR_XPOSE_LD;
           auto coop_accumulate = [&](const float *row, bool add) {
             const unsigned long long mine = reinterpret_cast<unsigned long long>(row);
+            const int j = lane & 3;
+            // all 16 loads of this lane in flight at once: frames (lane/4) + 8i, dims 16b + 4j
+            float4 vb[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float *src =
+                  reinterpret_cast<const float *>(__shfl_sync(0xffffffffu, mine, (lane >> 2) + 8 * i));
+#pragma unroll
+              for (int b = 0; b < d / 16; ++b) vb[4 * b + i] = __ldg(reinterpret_cast<const float4 *>(src + 16 * b + 4 * j));
+            }
 #pragma unroll
             for (int b = 0; b < d / 16; ++b) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int f = (lane >> 2) + 8 * i, j = lane & 3;
-                const float *src = reinterpret_cast<const float *>(__shfl_sync(0xffffffffu, mine, f));
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(src + 16 * b + 4 * j));
-                *reinterpret_cast<float4 *>(xs + f * SR_XPOSE_LD + 4 * j) = v;
-              }
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4 *>(xs + ((lane >> 2) + 8 * i) * SR_XPOSE_LD + 4 * j) = vb[4 * b + i];
               __syncwarp();
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
