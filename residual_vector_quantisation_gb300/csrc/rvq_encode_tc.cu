@@ -240,62 +240,97 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 
 // ===========================================================================
 // step 2: the stage loop in code space.
-// CTA item: one tile of 128 frames; two CTAs share each SM's tensor core, so
-// one CTA's stage boundaries and distance scans overlap the other's MMAs.
-// The query tile (A operand, hi and lo) lives in TMEM, written by the row
-// threads with tcgen05.st; shared memory holds only a ring of codebook
-// half-chunks: 128 codewords of -2*c, hi or lo, pre-swizzled, 32 KB per bulk
-// copy.  TMEM (256 columns): [0,64) A hi, [64,128) A lo, [128,256) distances.
-// Warps: 0 bulk-copy producer, 1 MMA issuer (+ TMEM owner), 2-5 one thread per
-// frame row: build the stage's query, then scan the distances.
+// CTA item: two tiles of 128 frames that walk the same codebook chunks, so
+// every chunk brought into shared memory feeds both (half the L2 traffic of
+// one tile per copy).  The two tiles' MMA issuers take turns chunk by chunk,
+// so the tensor core works on one tile's chunk while the other tile scans its
+// distances.
+//   * a ring of three half-chunks, one 32 KB bulk copy each (a bulk copy takes
+//     about the same time whatever its size, so copies are large): a chunk is
+//     128 codewords of -2*c as four atoms of 128 rows x 128 B, pre-swizzled --
+//     hi dims 0-31, hi 32-63 (hi half), lo 0-31, lo 32-63 (lo half); the lo
+//     half is copied and used first;
+//   * per tile: the partial sum of the next query (32 KB) and a staging area
+//     for one row per frame (32 KB);
+//   * ||c||^2 of the last three chunks (512 B each, one bulk copy per chunk);
+//   * TMEM, 256 columns per tile: [0,64) query hi, [64,128) query lo,
+//     [128,256) distances;
+//   * warps: 0 producer (bulk copies), 1 and 10 MMA issuers of tiles 0 and 1,
+//     2-5 rows of tile 0, 6-9 rows of tile 1 (one thread per frame: build the
+//     query, scan the distances).
+// The query of stage q+1 is p = P0[n][q+1] - sum_{s<=q} G[q+1][s][code_s].
+// All of it but the last term is known while stage q is being scanned, so
+// the row warps gather those rows between distance chunks: 16-byte
+// asynchronous copies (four lanes per 64-byte row segment) into the staging
+// area, subtracted from the partial sum one chunk later (the P0 row is copied
+// straight into the partial); the stage boundary gathers only the one row of
+// the code just found.  Terms are added in the order s = 0, 1, ..., q.
 // ===========================================================================
-constexpr int SR_KC = 128;
-constexpr int SR_STAGES = 3;
-constexpr uint32_t SR_ATOM = 128 * 128;      // 128 rows x 128 B
-constexpr uint32_t SR_B_STAGE = 2 * SR_ATOM;  // [atom] = 32 KB
-constexpr int SR_THREADS = 192;
-constexpr uint32_t SR_TMEM_COLS = 256;
+constexpr int SR_KC = 128;                    // codewords per chunk (MMA N)
+constexpr uint32_t SR_ATOM = 128 * 128;       // 128 codewords x 128 B
+constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // one bulk copy: hi or lo part of a chunk
+constexpr int SR_SLOTS = 3;                   // half-chunks in the ring
+constexpr int SR_THREADS = 352;
+constexpr uint32_t SR_TMEM_COLS = 512;        // 256 per tile
+constexpr uint32_t SR_TILE_COLS = 256;
 constexpr uint32_t SR_A_HI = 0, SR_A_LO = 64, SR_ACC = 128;
 constexpr uint32_t SR_IDESC = idesc_tf32(128, SR_KC);
+constexpr uint32_t SR_RING_BYTES = SR_SLOTS * SR_HALF;
+constexpr uint32_t SR_PART_BYTES = 128 * kCodeDim * 4;  // per tile: [128 rows][16 float4 slots], slot ^ (row & 7)
+constexpr int SR_CN_SLOTS = 3;
+constexpr uint32_t SR_CN_BYTES = SR_KC * 4;              // ||c||^2 of one chunk
 
-constexpr int SR_MAX_K = 1024;  // codewords whose norms fit the per-stage smem copy (larger K reads global)
 struct SrBars {
-  uint64_t b_full[SR_STAGES], b_empty[SR_STAGES];
-  uint64_t a_ready, acc_full, acc_empty, drain;
+  uint64_t b_full[SR_SLOTS], b_empty[SR_SLOTS];
+  uint64_t cn_full[SR_CN_SLOTS], cn_free[SR_CN_SLOTS];
+  uint64_t a_ready[2], acc_full[2], acc_empty[2];
+  uint64_t turn[2];  // turn[t]: the other tile's issuer has issued most of its chunk
+  uint64_t drain[2];
   uint32_t tmem;
+  uint32_t pad;
 };
-constexpr size_t SR_CN_BYTES = SR_MAX_K * 4;        // ||c||^2 of the current stage
-constexpr int SR_XPOSE_LD = 20;                       // floats per row of a warp's transpose scratch (16 + pad)
-constexpr size_t SR_XPOSE_BYTES = 4 * 32 * SR_XPOSE_LD * 4;  // 4 row warps x 32 frames
-constexpr size_t SR_SMEM = 1024 + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + SR_XPOSE_BYTES + sizeof(SrBars);
+// ring, partials, staging, norms, barriers
+constexpr size_t SR_SMEM = 1024 + SR_RING_BYTES + 4 * SR_PART_BYTES + SR_CN_SLOTS * SR_CN_BYTES + sizeof(SrBars);
+static_assert(SR_SMEM <= 227 * 1024, "search kernel shared memory");
 
-__global__ void __launch_bounds__(SR_THREADS, 2)
+__global__ void __launch_bounds__(SR_THREADS, 1)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
-                int n_items, int *__restrict__ status) {
+                int n_tiles, int *__restrict__ status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
-  float *cn_smem = reinterpret_cast<float *>(smem + SR_STAGES * SR_B_STAGE);
-  float *xpose = reinterpret_cast<float *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES);
-  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_STAGES * SR_B_STAGE + SR_CN_BYTES + SR_XPOSE_BYTES);
+  unsigned char *ring = smem;
+  float *cn_buf = reinterpret_cast<float *>(smem + SR_RING_BYTES + 4 * SR_PART_BYTES);
+  SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_RING_BYTES + 4 * SR_PART_BYTES + SR_CN_SLOTS * SR_CN_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkc = K / SR_KC;
-  // Every CTA walks the same codebook chunks; starting each CTA at a different
+  // tiles of this CTA: blockIdx.x + 2Gk as tile 0 and blockIdx.x + G + 2Gk as
+  // tile 1 (G = gridDim.x); a launch with no more tiles than CTAs thus puts
+  // one tile on each SM
+  const int sweep = 2 * gridDim.x;
+  // Every CTA walks the same codebook chunks; starting each at a different
   // chunk spreads the simultaneous bulk copies over nkc chunks of L2 instead
   // of one hot chunk.  The argmin merge below is order-independent.
   const int rot = blockIdx.x % nkc;
   constexpr int d = kCodeDim;
 
   if (tid == 0) {
-    for (int s = 0; s < SR_STAGES; ++s) {
+    for (int s = 0; s < SR_SLOTS; ++s) {
       mbar_init(&bar.b_full[s], 1);
-      mbar_init(&bar.b_empty[s], 1);
+      mbar_init(&bar.b_empty[s], 2);  // one commit per tile's MMA issuer
     }
-    mbar_init(&bar.a_ready, 128);
-    mbar_init(&bar.acc_full, 1);
-    mbar_init(&bar.acc_empty, 128);
-    mbar_init(&bar.drain, 1);
+    for (int s = 0; s < SR_CN_SLOTS; ++s) {
+      mbar_init(&bar.cn_full[s], 1);
+      mbar_init(&bar.cn_free[s], 256);  // every row thread of both tiles has scanned the chunk
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar.a_ready[t], 128);
+      mbar_init(&bar.acc_full[t], 1);
+      mbar_init(&bar.acc_empty[t], 128);
+      mbar_init(&bar.drain[t], 1);
+      mbar_init(&bar.turn[t], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -308,151 +343,207 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
   const uint32_t tmem = bar.tmem;
 
   if (warp == 0) {
-    // ---------------- producer: codebook half-chunk images ----------------
+    // ---------------- producer: two bulk copies per codebook chunk ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t hc = 0, ch = 0;  // half-chunks and norm blocks issued
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
+      for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep)
         for (int q = 0; q < n_q && ok; ++q)
-          for (int c = 0; c < nkc && ok; ++c)
-            for (int h = 0; h < 2; ++h, ++it) {
-              const int cr = (c + rot) % nkc;
-              const int s = it % SR_STAGES;
-              const uint32_t use = it / SR_STAGES;
+          for (int c = 0; c < nkc && ok; ++c) {
+            const int cr = (c + rot) % nkc;
+            for (int h = 1; h >= 0 && ok; --h) {  // lo half first: the order the MMAs use them
+              const int s = hc % SR_SLOTS;
+              const uint32_t use = hc / SR_SLOTS;
               if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
                 record_error(status, RVQ_DEVICE_TIMEOUT);
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&bar.b_full[s], SR_B_STAGE);
-              const float *src = cb_img + ((((size_t)q * nkc + cr) * 2 + h) * SR_B_STAGE) / 4;
-              bulk_g2s(smem + s * SR_B_STAGE, src, SR_B_STAGE, &bar.b_full[s]);
+              mbar_arrive_expect_tx(&bar.b_full[s], SR_HALF);
+              bulk_g2s(ring + s * SR_HALF, cb_img + (((size_t)q * nkc + cr) * 2 + h) * (SR_HALF / 4), SR_HALF,
+                       &bar.b_full[s]);
+              ++hc;
             }
-      for (uint32_t k = 0; k < SR_STAGES && k < it; ++k) {
-        const uint32_t j = it - 1 - k;
-        mbar_wait(&bar.b_full[j % SR_STAGES], (j / SR_STAGES) & 1);
+            if (!ok) break;
+            // the chunk's squared norms; the slot last held chunk ch - 3
+            const int sn = ch % SR_CN_SLOTS;
+            if (ch >= SR_CN_SLOTS && !mbar_wait(&bar.cn_free[sn], (ch / SR_CN_SLOTS - 1) & 1)) {
+              record_error(status, RVQ_DEVICE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar.cn_full[sn], SR_CN_BYTES);
+            bulk_g2s(cn_buf + sn * SR_KC, cnorm + (size_t)q * K + cr * SR_KC, SR_CN_BYTES, &bar.cn_full[sn]);
+            ++ch;
+          }
+      // the copies still in flight land before the CTA may exit
+      for (uint32_t k = 0; k < SR_SLOTS && k < hc; ++k) {
+        const uint32_t j = hc - 1 - k;
+        mbar_wait(&bar.b_full[j % SR_SLOTS], (j / SR_SLOTS) & 1);
+      }
+      for (uint32_t k = 0; k < SR_CN_SLOTS && k < ch; ++k) {
+        const uint32_t j = ch - 1 - k;
+        mbar_wait(&bar.cn_full[j % SR_CN_SLOTS], (j / SR_CN_SLOTS) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 || warp == 10) {
+    // ---------------- MMA issuers: warp 1 for tile 0, warp 10 for tile 1 ----------------
+    // An issuing thread that waits on an mbarrier stalls until its queued MMAs
+    // have drained, which would leave the tensor core idle; with one issuer per
+    // tile, each does its waits while the other tile's MMAs are queued.  The
+    // two take turns chunk by chunk (tile 0, tile 1, tile 0, ...): an issuer
+    // hands over the turn after 16 of its 24 MMAs, so the next tile's MMAs
+    // queue up behind the last ones without a gap, and the tile that has just
+    // finished scans its distances while the tensor core works on the other.
+    // The 24 MMAs of a tile-chunk are issued straight-line (compile-time
+    // operand offsets and accumulate flags) so that one thread keeps pace with
+    // the tensor core.  Both issuers commit to a chunk's empty barrier (count
+    // 2) per half-chunk; a tile 0 without a partner tile commits twice and
+    // takes no turns.
+    const int t = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      uint32_t it = 0, cc = 0, builds = 0;
+      uint32_t it = 0, builds = 0;
       bool ok = true;
       auto wait_or_fail = [&](uint64_t *b, uint32_t parity) {
-        if (!mbar_wait(b, parity)) {
+        if (ok && !mbar_wait(b, parity)) {
           record_error(status, RVQ_DEVICE_TIMEOUT);
           ok = false;
         }
         return ok;
       };
-      // descriptor of the smem base; operand descriptors add (byte offset >> 4)
-      const uint64_t desc0 = smem_desc(smem_addr(smem), 16, 1024, kSwizzle128B);
-      auto dB = [&](int s, int ks) {
-        return desc0 + (uint64_t)((s * SR_B_STAGE + (ks >> 2) * SR_ATOM + (ks & 3) * 32) >> 4);
-      };
-      const uint32_t acc = tmem + SR_ACC;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x)
+      // descriptor of the ring base; an operand adds (byte offset >> 4)
+      const uint64_t desc0 = smem_desc(smem_addr(ring), 16, 1024, kSwizzle128B);
+      const uint32_t tb = tmem + t * SR_TILE_COLS;
+      for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep) {
+        const bool pair = t0 + (int)gridDim.x < n_tiles;  // tile 1 present in this item
+        if (t == 1 && !pair) break;
         for (int q = 0; q < n_q && ok; ++q, ++builds)
-          for (int c = 0; c < nkc && ok; ++c, ++cc) {
-            if (cc > 0 && !wait_or_fail(&bar.acc_empty, (cc - 1) & 1)) break;
-            // hi half: a_hi . b_hi + a_lo . b_hi
-            int s = it % SR_STAGES;
-            if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
-            if (c == 0 && !wait_or_fail(&bar.a_ready, builds & 1)) break;
+          for (int c = 0; c < nkc && ok; ++c, ++it) {
+            const uint32_t j0 = 2 * it, j1 = j0 + 1;  // the chunk's lo and hi half-chunks
+            const int s0 = j0 % SR_SLOTS, s1 = j1 % SR_SLOTS;
+            if (it > 0 && !wait_or_fail(&bar.acc_empty[t], (it - 1) & 1)) break;
+            if (c == 0 && !wait_or_fail(&bar.a_ready[t], builds & 1)) break;
+            if (!wait_or_fail(&bar.b_full[s0], (j0 / SR_SLOTS) & 1)) break;
+            // turn: tile 1 follows tile 0's chunk `it`; tile 0 follows tile 1's chunk it - 1
+            if (pair && (t == 1 || it > 0) && !wait_or_fail(&bar.turn[t], (t == 1 ? it : it - 1) & 1)) break;
             tc_fence_after();
+            const uint64_t bd_lo = desc0 + (uint64_t)((s0 * SR_HALF) >> 4);
+            const uint64_t bd_hi = desc0 + (uint64_t)((s1 * SR_HALF) >> 4);
+            // lo half first (a_hi.b_lo, 8 MMAs), then hi (a_hi.b_hi + a_lo.b_hi, 16): the
+            // lo half's slot is freed early, and the next chunk's hi half, copied
+            // into it, is needed only a third of the way into that chunk
 #pragma unroll
-            for (int ks = 0; ks < d / 8; ++ks) {
-              const uint64_t bh = dB(s, ks);
-              mma_tf32_ta(acc, tmem + SR_A_HI + ks * 8, bh, SR_IDESC, ks ? 1u : 0u);
-              mma_tf32_ta(acc, tmem + SR_A_LO + ks * 8, bh, SR_IDESC, 1u);
+            for (int step = 0; step < 4; ++step) {
+              const bool hi = step >= 2;
+              if (step == 2) {
+                mma_commit(&bar.b_empty[s0]);  // the lo half is free once these MMAs are done
+                if (!pair) mma_commit(&bar.b_empty[s0]);
+                if (!wait_or_fail(&bar.b_full[s1], (j1 / SR_SLOTS) & 1)) break;
+                tc_fence_after();
+              }
+              if (step == 3) mbar_arrive(&bar.turn[1 - t]);  // 16 of 24 issued: hand over
+              const uint64_t bd = (hi ? bd_hi : bd_lo) + (uint64_t)(((step & 1) * SR_ATOM) >> 4);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t b = bd + (uint64_t)((ks * 32) >> 4);
+                const uint32_t ka = (uint32_t)((step & 1) * 4 + ks) * 8;
+                mma_tf32_ta(tb + SR_ACC, tb + SR_A_HI + ka, b, SR_IDESC, (step == 0 && ks == 0) ? 0u : 1u);
+                if (hi) mma_tf32_ta(tb + SR_ACC, tb + SR_A_LO + ka, b, SR_IDESC, 1u);
+              }
             }
-            mma_commit(&bar.b_empty[s]);
-            ++it;
-            // lo half: a_hi . b_lo
-            s = it % SR_STAGES;
-            if (!wait_or_fail(&bar.b_full[s], (it / SR_STAGES) & 1)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < d / 8; ++ks) mma_tf32_ta(acc, tmem + SR_A_HI + ks * 8, dB(s, ks), SR_IDESC, 1u);
-            mma_commit(&bar.acc_full);
-            mma_commit(&bar.b_empty[s]);
-            ++it;
+            mma_commit(&bar.acc_full[t]);
+            mma_commit(&bar.b_empty[s1]);
+            if (!pair) mma_commit(&bar.b_empty[s1]);
           }
-      mma_commit(&bar.drain);
-      mbar_wait(&bar.drain, 0);
+      }
+      mma_commit(&bar.drain[t]);
+      mbar_wait(&bar.drain[t], 0);
     }
   } else {
-    // ---------------- one thread per frame row (warps 2..5) ----------------
-    // Stage q's query is p_q = P0[n][q] - sum_{s<q} G[q][s][code_s], built
-    // between stages (the co-resident CTA keeps the tensor core busy meanwhile).
-    const int quarter = warp & 3;       // TMEM lane quarter of this warp
-    const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
-    const int rt = tid - 64;            // 0..127
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    // ---------------- one thread per frame row (warps 2-9) ----------------
+    const int tile = (warp - 2) >> 2;  // 0 or 1
+    const int quarter = warp & 3;      // TMEM lane quarter of this warp
+    const uint32_t lane_base = tmem + tile * SR_TILE_COLS + ((uint32_t)(quarter * 32) << 16);
     const int64_t ld = (int64_t)n_q * d;
-    const bool cn_in_smem = K <= SR_MAX_K;
-    uint32_t cc = 0, stage_count = 0;
+    float4 *wpart = reinterpret_cast<float4 *>(smem + SR_RING_BYTES + tile * SR_PART_BYTES) + quarter * 32 * (d / 4);
+    float4 *wstage =
+        reinterpret_cast<float4 *>(smem + SR_RING_BYTES + (2 + tile) * SR_PART_BYTES) + quarter * 32 * (d / 4);
+    const int f0 = lane >> 2, j = lane & 3;       // cooperative layout: frames f0 + 8i, slots 4b + j
+    uint64_t *acc_full = &bar.acc_full[tile], *acc_empty = &bar.acc_empty[tile], *a_ready = &bar.a_ready[tile];
+    uint32_t cc = 0;
     bool ok = true;
     int my_codes[kMaxStages];
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int64_t n = (int64_t)item * 128 + r;
+
+    // Term rows: one 64-float row per frame of this warp (`mine` is this
+    // thread's frame's row), copied asynchronously in the cooperative layout;
+    // each lane later reads back only the pieces it copied itself.  A first
+    // term lands straight in the partial sum, any other in the staging area.
+    bool pending = false, pending_first = false;
+    auto term_issue = [&](const float *mine, bool first) {
+      const unsigned long long m = reinterpret_cast<unsigned long long>(mine);
+      float4 *dst = first ? wpart : wstage;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 *src = reinterpret_cast<const float4 *>(__shfl_sync(0xffffffffu, m, f0 + 8 * i));
+#pragma unroll
+        for (int b = 0; b < 4; ++b) cp_async16(dst + (f0 + 8 * i) * (d / 4) + ((4 * b + j) ^ f0), src + 4 * b + j);
+      }
+      cp_async_commit();
+      pending = true;
+      pending_first = first;
+    };
+    // wait for this thread's copies; partial -= staged rows
+    auto term_finish = [&]() {
+      cp_async_wait_all();
+      if (!pending_first) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int idx = (f0 + 8 * i) * (d / 4) + ((4 * b + j) ^ f0);
+            float4 t = wpart[idx];
+            const float4 v = wstage[idx];
+            t.x -= v.x;
+            t.y -= v.y;
+            t.z -= v.z;
+            t.w -= v.w;
+            wpart[idx] = t;
+          }
+      }
+      pending = false;
+    };
+
+    int my_tile = blockIdx.x + tile * gridDim.x;
+    if (my_tile < n_tiles) {  // the first query's partial: the projection row itself
+      const int64_t n = (int64_t)my_tile * 128 + quarter * 32 + lane;
+      term_issue(P0 + (n < n_rows ? n : 0) * ld, true);
+    }
+    for (; my_tile < n_tiles && ok; my_tile += sweep) {
+      const int64_t n = (int64_t)my_tile * 128 + quarter * 32 + lane;
       const bool valid = n < n_rows;
-      for (int q = 0; q < n_q && ok; ++q, ++stage_count) {
-        // ---- query p_q = P0[n][q] - sum_{s<q} G[q][s][code_s], rows read cooperatively:
-        //      four lanes read 64 contiguous bytes of one frame's row (8 rows per warp
-        //      instruction), and a per-warp shared-memory transpose hands every lane
-        //      its own frame's 64 values.  Terms are added in the same order as a
-        //      plain per-thread sum.
+      const int64_t n_next = n + (int64_t)sweep * 128;
+      const bool has_next = my_tile + sweep < n_tiles;
+      // a tile 0 without a partner tile releases the norm blocks for both
+      const bool alone = tile == 0 && my_tile + (int)gridDim.x >= n_tiles;
+      for (int q = 0; q < n_q && ok; ++q) {
+        // ---- stage boundary: the last term of the query, then the A operand
+        if (pending) term_finish();
+        if (q > 0) {
+          term_issue(G + ((size_t)pair_index(q, q - 1) * K + my_codes[q - 1]) * d, false);
+          term_finish();
+        }
+        __syncwarp();
         {
           float p[d];
 #pragma unroll
-          for (int u = 0; u < d; ++u) p[u] = 0.f;
-          float *xs = xpose + (warp - 2) * 32 * SR_XPOSE_LD;
-          auto coop_accumulate = [&](const float *row, bool add) {
-            const unsigned long long mine = reinterpret_cast<unsigned long long>(row);
-            const int j = lane & 3;
-            // all 16 loads of this lane in flight at once: frames (lane/4) + 8i, dims 16b + 4j
-            float4 vb[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float *src =
-                  reinterpret_cast<const float *>(__shfl_sync(0xffffffffu, mine, (lane >> 2) + 8 * i));
-#pragma unroll
-              for (int b = 0; b < d / 16; ++b) vb[4 * b + i] = __ldg(reinterpret_cast<const float4 *>(src + 16 * b + 4 * j));
-            }
-#pragma unroll
-            for (int b = 0; b < d / 16; ++b) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4 *>(xs + ((lane >> 2) + 8 * i) * SR_XPOSE_LD + 4 * j) = vb[4 * b + i];
-              __syncwarp();
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float4 v = *reinterpret_cast<const float4 *>(xs + lane * SR_XPOSE_LD + 4 * u);
-                if (add) {
-                  p[16 * b + 4 * u] += v.x;
-                  p[16 * b + 4 * u + 1] += v.y;
-                  p[16 * b + 4 * u + 2] += v.z;
-                  p[16 * b + 4 * u + 3] += v.w;
-                } else {
-                  p[16 * b + 4 * u] -= v.x;
-                  p[16 * b + 4 * u + 1] -= v.y;
-                  p[16 * b + 4 * u + 2] -= v.z;
-                  p[16 * b + 4 * u + 3] -= v.w;
-                }
-              }
-              __syncwarp();
-            }
-          };
-          // invalid frames read a valid row and discard the result
-          coop_accumulate(P0 + (valid ? n : 0) * ld + q * d, true);
-          for (int s = 0; s < q; ++s)
-            coop_accumulate(G + (pair_index(q, s) * K + (valid ? my_codes[s] : 0)) * d, false);
-          if (!valid) {
-#pragma unroll
-            for (int u = 0; u < d; ++u) p[u] = 0.f;
+          for (int u = 0; u < d / 4; ++u) {
+            const float4 t = wpart[lane * (d / 4) + (u ^ (lane & 7))];
+            p[4 * u] = t.x;
+            p[4 * u + 1] = t.y;
+            p[4 * u + 2] = t.z;
+            p[4 * u + 3] = t.w;
           }
-          // A operand: raw (= hi after TF32 truncation) and lo parts into this row's TMEM lane
+          // raw (= hi after TF32 truncation) and lo parts into this row's TMEM lane
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float lo[32];
@@ -466,31 +557,25 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&bar.a_ready);
+          mbar_arrive(a_ready);
         }
-        // the next stage's projections do not depend on this stage's code: pull them into L2 now
-        if (valid && q + 1 < n_q) {
-          const float *nxt = P0 + n * ld + (q + 1) * d;
-          prefetch_l2(nxt);
-          prefetch_l2(nxt + 32);
-        }
-        // ---- this stage's squared norms into smem, between two barriers of the row
-        //      threads (every row thread has finished the previous stage's scan)
-        const float *cnq = cnorm + (int64_t)q * K;
-        float *cns = cn_smem;
-        if (cn_in_smem) {
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          for (int e = rt * 4; e < K; e += 128 * 4)
-            *reinterpret_cast<float4 *>(cns + e) = __ldg(reinterpret_cast<const float4 *>(cnq + e));
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-        }
-        const float *cnsrc = cn_in_smem ? cns : cnq;
+        __syncwarp();  // every lane has read its row before the next query's terms overwrite it
+        // ---- terms of the next query known before this stage's code:
+        //      next stage: P0[n][q+1], G[q+1][0..q-1];  next tile: P0[n'][0]
+        const int q_next = q + 1 < n_q ? q + 1 : 0;
+        const int n_terms = q + 1 < n_q ? q + 1 : (has_next ? 1 : 0);
+        const int64_t n_row = q + 1 < n_q ? (valid ? n : 0) : (n_next < n_rows ? n_next : 0);
+        auto term_row = [&](int t) -> const float * {
+          return t == 0 ? P0 + n_row * ld + q_next * d
+                        : G + ((size_t)pair_index(q_next, t - 1) * K + my_codes[t - 1]) * d;
+        };
+        int done = 0;
         // ---- scan the K distances ||c||^2 - 2 p.c; keep the lexicographic (value, index) minimum
         float best_v = __int_as_float(0x7f800000);
         int best_k = 0;
         for (int c = 0; c < nkc; ++c, ++cc) {
           const int cr = (c + rot) % nkc;
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full, cc & 1))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(acc_full, cc & 1))) {
             record_error(status, RVQ_DEVICE_TIMEOUT);
             ok = false;
             break;
@@ -502,8 +587,14 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
             tmem_ld32(lane_base + SR_ACC + g * 32, *reinterpret_cast<float(*)[32]>(&v[32 * g]));
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(&bar.acc_empty);  // the accumulator is free: the values are in registers
-          const float4 *cn4 = reinterpret_cast<const float4 *>(cnsrc + cr * SR_KC);
+          mbar_arrive(acc_empty);  // the accumulator is free: the values are in registers
+          const int sn = cc % SR_CN_SLOTS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.cn_full[sn], (cc / SR_CN_SLOTS) & 1))) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const float4 *cn4 = reinterpret_cast<const float4 *>(cn_buf + sn * SR_KC);
 #pragma unroll
           for (int u = 0; u < SR_KC / 4; ++u) {
             const float4 cn = cn4[u];
@@ -520,6 +611,8 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
 #pragma unroll
             for (int i = 0; i < w2; ++i) mm[i] = fminf(mm[i], mm[i + w2]);
           const float m = mm[0];
+          mbar_arrive(&bar.cn_free[sn]);  // the norms are in registers
+          if (alone) mbar_arrive(&bar.cn_free[sn]);
           if (m <= best_v) {  // rare after the first chunks: locate the first index holding m
             int first = SR_KC - 1;
 #pragma unroll
@@ -530,6 +623,14 @@ __global__ void __launch_bounds__(SR_THREADS, 2)
               best_v = m;
               best_k = k;
             }
+          }
+          // ---- this chunk's share of the next query's known terms, in order:
+          //      the previous one is added now, the new one stays in flight
+          //      until after the next chunk's scan
+          const int target = (n_terms * (c + 1) + nkc - 1) / nkc;
+          for (; done < target; ++done) {
+            if (pending) term_finish();
+            term_issue(term_row(done), done == 0);
           }
         }
         if (!ok) break;
@@ -627,7 +728,7 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
       tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int tiles = (int)((n + 127) / 128);
-  k_search_tc<<<tiles < 2 * sms ? tiles : 2 * sms, SR_THREADS, SR_SMEM, st>>>(
+  k_search_tc<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(
       p0, at<float>(tables, L.g), at<float>(tables, L.cb_img), at<float>(tables, L.cnorm), codes + n0 * n_q, n, n_q,
       K, tiles, status);
   return cudaGetLastError();
