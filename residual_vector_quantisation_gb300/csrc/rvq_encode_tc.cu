@@ -255,9 +255,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 //   * ||c||^2 of the last three chunks (512 B each, one bulk copy per chunk);
 //   * TMEM, 256 columns per tile: [0,64) query hi, [64,128) query lo,
 //     [128,256) distances;
-//   * warps: 0 producer (bulk copies), 1 and 10 MMA issuers of tiles 0 and 1,
-//     2-5 rows of tile 0, 6-9 rows of tile 1 (one thread per frame: build the
-//     query, scan the distances).
+//   * warps: 0 and 11 producers (bulk copies), 1 and 10 MMA issuers of tiles 0
+//     and 1, 2-5 rows of tile 0, 6-9 rows of tile 1 (one thread per frame:
+//     build the query, scan the distances).
 // The query of stage q+1 is p = P0[n][q+1] - sum_{s<=q} G[q+1][s][code_s].
 // All of it but the last term is known while stage q is being scanned, so
 // the row warps gather those rows between distance chunks: 16-byte
@@ -270,7 +270,7 @@ constexpr int SR_KC = 128;                    // codewords per chunk (MMA N)
 constexpr uint32_t SR_ATOM = 128 * 128;       // 128 codewords x 128 B
 constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // one bulk copy: hi or lo part of a chunk
 constexpr int SR_SLOTS = 3;                   // half-chunks in the ring
-constexpr int SR_THREADS = 352;
+constexpr int SR_THREADS = 384;
 constexpr uint32_t SR_TMEM_COLS = 512;        // 256 per tile
 constexpr uint32_t SR_TILE_COLS = 256;
 constexpr uint32_t SR_A_HI = 0, SR_A_LO = 64, SR_ACC = 128;
@@ -342,29 +342,31 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem;
 
-  if (warp == 0) {
-    // ---------------- producer: two bulk copies per codebook chunk ----------------
+  if (warp == 0 || warp == 11) {
+    // ---------------- producers: warp 0 the lo halves and norms, warp 11 the hi halves ----------------
+    // A thread's bulk copies are carried out one after another (about a third
+    // of a microsecond each, whatever their size), so the hi halves, which
+    // are waited for just in time, get a producer of their own.
+    const int h = warp == 0 ? 1 : 0;
     if (lane == 0) {
-      uint32_t hc = 0, ch = 0;  // half-chunks and norm blocks issued
+      uint32_t ch = 0;  // chunks gone through
       bool ok = true;
       for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep)
         for (int q = 0; q < n_q && ok; ++q)
-          for (int c = 0; c < nkc && ok; ++c) {
+          for (int c = 0; c < nkc && ok; ++c, ++ch) {
             const int cr = (c + rot) % nkc;
-            for (int h = 1; h >= 0 && ok; --h) {  // lo half first: the order the MMAs use them
-              const int s = hc % SR_SLOTS;
-              const uint32_t use = hc / SR_SLOTS;
-              if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
-                record_error(status, RVQ_DEVICE_TIMEOUT);
-                ok = false;
-                break;
-              }
-              mbar_arrive_expect_tx(&bar.b_full[s], SR_HALF);
-              bulk_g2s(ring + s * SR_HALF, cb_img + (((size_t)q * nkc + cr) * 2 + h) * (SR_HALF / 4), SR_HALF,
-                       &bar.b_full[s]);
-              ++hc;
+            const uint32_t j = 2 * ch + (1 - h);  // half-chunk index: lo halves even, hi halves odd
+            const int s = j % SR_SLOTS;
+            const uint32_t use = j / SR_SLOTS;
+            if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
+              record_error(status, RVQ_DEVICE_TIMEOUT);
+              ok = false;
+              break;
             }
-            if (!ok) break;
+            mbar_arrive_expect_tx(&bar.b_full[s], SR_HALF);
+            bulk_g2s(ring + s * SR_HALF, cb_img + (((size_t)q * nkc + cr) * 2 + h) * (SR_HALF / 4), SR_HALF,
+                     &bar.b_full[s]);
+            if (h == 0) continue;
             // the chunk's squared norms; the slot last held chunk ch - 3
             const int sn = ch % SR_CN_SLOTS;
             if (ch >= SR_CN_SLOTS && !mbar_wait(&bar.cn_free[sn], (ch / SR_CN_SLOTS - 1) & 1)) {
@@ -374,16 +376,14 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             }
             mbar_arrive_expect_tx(&bar.cn_full[sn], SR_CN_BYTES);
             bulk_g2s(cn_buf + sn * SR_KC, cnorm + (size_t)q * K + cr * SR_KC, SR_CN_BYTES, &bar.cn_full[sn]);
-            ++ch;
           }
-      // the copies still in flight land before the CTA may exit
-      for (uint32_t k = 0; k < SR_SLOTS && k < hc; ++k) {
-        const uint32_t j = hc - 1 - k;
-        mbar_wait(&bar.b_full[j % SR_SLOTS], (j / SR_SLOTS) & 1);
-      }
-      for (uint32_t k = 0; k < SR_CN_SLOTS && k < ch; ++k) {
-        const uint32_t j = ch - 1 - k;
-        mbar_wait(&bar.cn_full[j % SR_CN_SLOTS], (j / SR_CN_SLOTS) & 1);
+      // Every copy is waited for by the threads that use it before the final
+      // barrier; after an error, the last copy of this thread (whose slot no
+      // later copy can have reused) still lands before the CTA may exit.
+      if (ch > 0) {
+        const uint32_t jj = 2 * (ch - 1) + (1 - h);
+        mbar_wait(&bar.b_full[jj % SR_SLOTS], (jj / SR_SLOTS) & 1);
+        if (h == 1) mbar_wait(&bar.cn_full[(ch - 1) % SR_CN_SLOTS], ((ch - 1) / SR_CN_SLOTS) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     // have drained, which would leave the tensor core idle; with one issuer per
     // tile, each does its waits while the other tile's MMAs are queued.  The
     // two take turns chunk by chunk (tile 0, tile 1, tile 0, ...): an issuer
-    // hands over the turn after 16 of its 24 MMAs, so the next tile's MMAs
+    // hands over the turn after 20 of its 24 MMAs, so the next tile's MMAs
     // queue up behind the last ones without a gap, and the tile that has just
     // finished scans its distances while the tensor core works on the other.
     // The 24 MMAs of a tile-chunk are issued straight-line (compile-time
@@ -441,10 +441,10 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
                 if (!wait_or_fail(&bar.b_full[s1], (j1 / SR_SLOTS) & 1)) break;
                 tc_fence_after();
               }
-              if (step == 3) mbar_arrive(&bar.turn[1 - t]);  // 16 of 24 issued: hand over
               const uint64_t bd = (hi ? bd_hi : bd_lo) + (uint64_t)(((step & 1) * SR_ATOM) >> 4);
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
+                if (step == 3 && ks == 2) mbar_arrive(&bar.turn[1 - t]);  // 20 of 24 issued: hand over
                 const uint64_t b = bd + (uint64_t)((ks * 32) >> 4);
                 const uint32_t ka = (uint32_t)((step & 1) * 4 + ks) * 8;
                 mma_tf32_ta(tb + SR_ACC, tb + SR_A_HI + ka, b, SR_IDESC, (step == 0 && ks == 0) ? 0u : 1u);
