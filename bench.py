@@ -37,6 +37,9 @@ import rvq_inputs as ri  # noqa: E402
 
 WORKLOAD = "large_batch"
 METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of k_project_tc (209.8 MB)
+# and k_search_tc (94.9 MB) over 38 912 frames of large_batch.
+ENCODE_DRAM_BYTES_PER_FRAME = {"large_batch": (209.8e6 + 94.9e6) / 38912}
 L2_BYTES = 129 * 2 ** 20
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
@@ -268,6 +271,10 @@ def e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev):
 def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, clocks, world):
     peaks = _peaks()
     clk = clocks.summary()
+    # DRAM bytes (read + write) per frame of one encode call, k_project_tc +
+    # k_search_tc, from one ncu capture of a one-wave case of this workload,
+    # scaled by frames; None for other workloads or once the kernels change.
+    enc_traffic = ENCODE_DRAM_BYTES_PER_FRAME.get(w.name)
     # encode: 3xTF32 tensor-core kernels.  The TF32 peak is the measured bf16
     # peak times the nominal dense tf32/bf16 ratio (1.1 / 2.25 PFLOP/s); three
     # TF32 passes make up one float32-accurate product, so the roofline for the
@@ -299,7 +306,8 @@ def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, cloc
         "encode_ms": enc_ms, "decode_ms": dec_ms,
         "encode_frames_per_s": N / (enc_ms / 1e3), "decode_frames_per_s": N / (dec_ms / 1e3),
         "roofline": {"bound": "tensor", "achieved": enc_achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": enc_achieved / tc_peak, "traffic": None,
+                     "frac": enc_achieved / tc_peak,
+                     "traffic": None if enc_traffic is None else enc_traffic * N,
                      "kernel": "encode: k_project_tc + k_search_tc (3xTF32 tcgen05), algorithmic FLOPs "
                                "Q*(2*D*d + 2*K*d) per frame",
                      "peak_basis": f"{peaks['source']} bf16 {peaks['bf16_tflops']:.1f} x 1.1/2.25 (tf32) / 3 passes",
