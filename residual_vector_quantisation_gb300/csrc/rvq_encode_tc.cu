@@ -38,15 +38,18 @@ using namespace ptx;
 // step 1: P0 = x . w_in^T + b_in
 // CTA item: 256 frames (two M=128 tiles) x 256 output columns, K = D in
 // slices of 16 floats (64-byte rows, 64-byte swizzle), 3-stage TMA ring.
-// Warps: 0 TMA producer, 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
+// Warps: 0 and 6 TMA producers (x tiles; w_in hi and lo tiles -- a thread's
+// copies are carried out one after another, so two threads issue them),
+// 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
 // ===========================================================================
 constexpr int PJ_BK = 16;
 constexpr int PJ_STAGES = 3;
 constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;          // 8 KB: one tile's K-slice
 constexpr uint32_t PJ_B = 256 * PJ_BK * 4;               // 16 KB
 constexpr uint32_t PJ_STAGE = 4 * PJ_A_TILE + 2 * PJ_B;  // raw[2] lo[2] bhi blo = 64 KB
-constexpr uint32_t PJ_TX = 2 * PJ_A_TILE + 2 * PJ_B;     // bytes TMA writes per stage
-constexpr int PJ_THREADS = 192;
+constexpr uint32_t PJ_TX_X = 2 * PJ_A_TILE;             // bytes each producer's TMA writes per stage
+constexpr uint32_t PJ_TX_W = 2 * PJ_B;
+constexpr int PJ_THREADS = 224;
 constexpr uint32_t PJ_IDESC = idesc_tf32(128, 256);
 
 struct PjBars {
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 
   if (tid == 0) {
     for (int s = 0; s < PJ_STAGES; ++s) {
-      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.full[s], 2);  // one arrival per producer
       mbar_init(&bar.conv[s], 128);
       mbar_init(&bar.empty[s], 1);
     }
@@ -97,8 +100,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers ----------------
+    const bool px = warp == 0;
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -112,11 +116,15 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bar.full[s], PJ_TX);
-          tma_load_2d(a_raw(s, 0), &tm_x, ks * PJ_BK, m0, &bar.full[s]);
-          tma_load_2d(a_raw(s, 1), &tm_x, ks * PJ_BK, m0 + 128, &bar.full[s]);
-          tma_load_2d(b_hi(s), &tm_whi, ks * PJ_BK, c0, &bar.full[s]);
-          tma_load_2d(b_lo(s), &tm_wlo, ks * PJ_BK, c0, &bar.full[s]);
+          if (px) {
+            mbar_arrive_expect_tx(&bar.full[s], PJ_TX_X);
+            tma_load_2d(a_raw(s, 0), &tm_x, ks * PJ_BK, m0, &bar.full[s]);
+            tma_load_2d(a_raw(s, 1), &tm_x, ks * PJ_BK, m0 + 128, &bar.full[s]);
+          } else {
+            mbar_arrive_expect_tx(&bar.full[s], PJ_TX_W);
+            tma_load_2d(b_hi(s), &tm_whi, ks * PJ_BK, c0, &bar.full[s]);
+            tma_load_2d(b_lo(s), &tm_wlo, ks * PJ_BK, c0, &bar.full[s]);
+          }
         }
       }
       // drain: the last load issued into each stage has landed before exit
