@@ -121,6 +121,22 @@ def test_moss_deep_workload_sampled():
     assert res["n_equal"] >= 0.97 * res["n_stages"]
 
 
+def test_k4096_q10_workload_sampled():
+    """Ten books of 4096 codewords: 32 distance chunks per stage and 45 G
+    tables; 2000 sampled frames (including both ends) checked on the oracle."""
+    w = ri.WORKLOAD_BY_NAME["k4096_q10"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    rvq = make_rvq(W)
+    xt = torch.from_numpy(x).to(DEV)
+    codes, x_hat = rvq.reconstruct(xt)
+    torch.cuda.synchronize()
+    rows = np.sort(np.concatenate([np.random.default_rng(3).choice(w.N - 2, 1998, replace=False) + 1, [0, w.N - 1]]))
+    res = check_encode(W, x, codes.cpu().numpy(), rows=rows, x_rms=rms(x), x_hat_gpu=x_hat.cpu().numpy(),
+                       label="k4096_q10")
+    assert res["n_equal"] >= 0.97 * res["n_stages"]
+
+
 def test_large_batch_workload_full_size_sampled():
     """192 000 frames encoded and decoded on the GPU exactly as the benchmark
     does; 3000 sampled frames (including both ends) checked on the oracle."""
