@@ -127,8 +127,9 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
 /* Scratch bytes rvq_encode / rvq_reconstruct need for n_frames frames at
  * depth n_q.  Scratch starts with a 256-byte header whose first int32 is a
  * device status word: each call sets it to 0, and a kernel sets it to 5 if
- * one of its bounded device waits gave up (that call's codes are then
- * invalid; read it after the stream reaches the call).  The rest holds the
+ * one of its bounded device waits gave up, or to 6 if it was launched in a
+ * shape it does not accept (an internal error); either way that call's codes
+ * are invalid (read it after the stream reaches the call).  The rest holds the
  * per-frame stage projections ([chunk][n_q*d] float32) of one chunk of
  * frames; encode works through the frames chunk by chunk.  This returns the
  * size for chunks of up to about 96 MiB of projections.  A larger scratch is

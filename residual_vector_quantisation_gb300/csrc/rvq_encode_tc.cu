@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // one tile per copy).  The two tiles' MMA issuers take turns chunk by chunk,
 // so the tensor core works on one tile's chunk while the other tile scans its
 // distances.
-//   * a ring of three half-chunks, one 32 KB bulk copy each (a bulk copy takes
+//   * a ring of three (split: five) half-chunks, one 32 KB bulk copy each (a bulk copy takes
 //     about the same time whatever its size, so copies are large): a chunk is
 //     128 codewords of -2*c as four atoms of 128 rows x 128 B, pre-swizzled --
 //     hi dims 0-31, hi 32-63 (hi half), lo 0-31, lo 32-63 (lo half); the lo
@@ -271,13 +271,27 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // the row warps gather those rows between distance chunks: 16-byte
 // asynchronous copies (four lanes per 64-byte row segment) into the staging
 // area, subtracted from the partial sum one chunk later (the P0 row is copied
-// straight into the partial); the stage boundary gathers only the one row of
-// the code just found.  Terms are added in the order s = 0, 1, ..., q.
+// straight into the partial); the stage boundary loads only the one row of
+// the code just found, straight into registers, and forms the query there.
+// Terms are added in the order s = 0, 1, ..., q.
+// A launch with no more tiles than SMs (the SPLIT variant, for a stage of an
+// even number of chunks) gives each CTA one tile and splits it: both
+// pipelines work on that tile, pipeline t taking the chunks c = t mod 2, so
+// the issuers still take turns.
+// Only pipeline 0 builds the query; both MMA issuers read it from pipeline
+// 0's TMEM columns, and tile 1's shared-memory areas become two more ring
+// slots.  At the end of a stage pipeline 1 hands its per-frame (value,
+// index) minimum to pipeline 0 through TMEM (two of its own query columns,
+// unused when split), and pipeline 0 keeps the lexicographic minimum of the
+// two.  (Otherwise a CTA's last item may hold one tile alone; it runs on
+// pipeline 0 with no turns.  It ends no later than the two-tile items of the
+// other CTAs, so splitting it would not shorten the launch.)
 // ===========================================================================
 constexpr int SR_KC = 128;                    // codewords per chunk (MMA N)
 constexpr uint32_t SR_ATOM = 128 * 128;       // 128 codewords x 128 B
 constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // one bulk copy: hi or lo part of a chunk
 constexpr int SR_SLOTS = 3;                   // half-chunks in the ring
+constexpr int SR_SLOTS_SPLIT = 5;             // ... when every item is split: plus tile 1's two areas
 constexpr int SR_THREADS = 384;
 constexpr uint32_t SR_TMEM_COLS = 512;        // 256 per tile
 constexpr uint32_t SR_TILE_COLS = 256;
@@ -289,18 +303,22 @@ constexpr int SR_CN_SLOTS = 3;
 constexpr uint32_t SR_CN_BYTES = SR_KC * 4;              // ||c||^2 of one chunk
 
 struct SrBars {
-  uint64_t b_full[SR_SLOTS], b_empty[SR_SLOTS];
+  uint64_t b_full[SR_SLOTS_SPLIT], b_empty[SR_SLOTS_SPLIT];
   uint64_t cn_full[SR_CN_SLOTS], cn_free[SR_CN_SLOTS];
   uint64_t a_ready[2], acc_full[2], acc_empty[2];
   uint64_t turn[2];  // turn[t]: the other tile's issuer has issued most of its chunk
   uint64_t drain[2];
+  uint64_t xch_full[2], xch_free[2];  // split items: pipeline 1's stage minima (in TMEM), double-buffered
   uint32_t tmem;
   uint32_t pad;
 };
-// ring, partials, staging, norms, barriers
+// ring, tile 1's partial and staging (the ring's slots 3 and 4 when every item
+// is split), tile 0's partial and staging, norms, barriers
+static_assert(SR_RING_BYTES + 2 * SR_PART_BYTES == SR_SLOTS_SPLIT * SR_HALF, "split ring");
 constexpr size_t SR_SMEM = 1024 + SR_RING_BYTES + 4 * SR_PART_BYTES + SR_CN_SLOTS * SR_CN_BYTES + sizeof(SrBars);
 static_assert(SR_SMEM <= 227 * 1024, "search kernel shared memory");
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(SR_THREADS, 1)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
@@ -313,18 +331,24 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   SrBars &bar = *reinterpret_cast<SrBars *>(smem + SR_RING_BYTES + 4 * SR_PART_BYTES + SR_CN_SLOTS * SR_CN_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkc = K / SR_KC;
-  // tiles of this CTA: blockIdx.x + 2Gk as tile 0 and blockIdx.x + G + 2Gk as
-  // tile 1 (G = gridDim.x); a launch with no more tiles than CTAs thus puts
-  // one tile on each SM
+  // tiles of this CTA: b + 2Bk as tile 0 and b + B + 2Bk as tile 1
+  // (b = blockIdx.x, B = gridDim.x); a launch with no more tiles than CTAs
+  // thus puts one tile on each SM, split between the CTA's two pipelines
   const int sweep = 2 * gridDim.x;
   // Every CTA walks the same codebook chunks; starting each at a different
   // chunk spreads the simultaneous bulk copies over nkc chunks of L2 instead
   // of one hot chunk.  The argmin merge below is order-independent.
   const int rot = blockIdx.x % nkc;
   constexpr int d = kCodeDim;
+  constexpr int SLOTS = SPLIT ? SR_SLOTS_SPLIT : SR_SLOTS;
+  // the split ring takes tile 1's areas: only for launches of one tile per CTA
+  if (SPLIT && (n_tiles > (int)gridDim.x || nkc % 2 != 0)) {
+    if (threadIdx.x == 0) record_error(status, RVQ_DEVICE_BAD_LAUNCH);
+    return;
+  }
 
   if (tid == 0) {
-    for (int s = 0; s < SR_SLOTS; ++s) {
+    for (int s = 0; s < SLOTS; ++s) {
       mbar_init(&bar.b_full[s], 1);
       mbar_init(&bar.b_empty[s], 2);  // one commit per tile's MMA issuer
     }
@@ -338,6 +362,8 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       mbar_init(&bar.acc_empty[t], 128);
       mbar_init(&bar.drain[t], 1);
       mbar_init(&bar.turn[t], 1);
+      mbar_init(&bar.xch_full[t], 128);
+      mbar_init(&bar.xch_free[t], 128);
     }
     fence_mbar_init();
   }
@@ -363,9 +389,9 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         for (int q = 0; q < n_q && ok; ++q)
           for (int c = 0; c < nkc && ok; ++c, ++ch) {
             const int cr = (c + rot) % nkc;
-            const uint32_t j = 2 * ch + (1 - h);  // half-chunk index: lo halves even, hi halves odd
-            const int s = j % SR_SLOTS;
-            const uint32_t use = j / SR_SLOTS;
+            const uint32_t j = 2 * ch + (1 - h);
+            const int s = j % SLOTS;
+            const uint32_t use = j / SLOTS;
             if (use > 0 && !mbar_wait(&bar.b_empty[s], (use - 1) & 1)) {
               record_error(status, RVQ_DEVICE_TIMEOUT);
               ok = false;
@@ -390,7 +416,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       // later copy can have reused) still lands before the CTA may exit.
       if (ch > 0) {
         const uint32_t jj = 2 * (ch - 1) + (1 - h);
-        mbar_wait(&bar.b_full[jj % SR_SLOTS], (jj / SR_SLOTS) & 1);
+        mbar_wait(&bar.b_full[jj % SLOTS], (jj / SLOTS) & 1);
         if (h == 1) mbar_wait(&bar.cn_full[(ch - 1) % SR_CN_SLOTS], ((ch - 1) / SR_CN_SLOTS) & 1);
       }
     }
@@ -399,18 +425,19 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     // An issuing thread that waits on an mbarrier stalls until its queued MMAs
     // have drained, which would leave the tensor core idle; with one issuer per
     // tile, each does its waits while the other tile's MMAs are queued.  The
-    // two take turns chunk by chunk (tile 0, tile 1, tile 0, ...): an issuer
-    // hands over the turn after 20 of its 24 MMAs, so the next tile's MMAs
-    // queue up behind the last ones without a gap, and the tile that has just
-    // finished scans its distances while the tensor core works on the other.
-    // The 24 MMAs of a tile-chunk are issued straight-line (compile-time
-    // operand offsets and accumulate flags) so that one thread keeps pace with
-    // the tensor core.  Both issuers commit to a chunk's empty barrier (count
-    // 2) per half-chunk; a tile 0 without a partner tile commits twice and
-    // takes no turns.
+    // two take turns chunk by chunk (tile 0, tile 1, tile 0, ...; in a split
+    // item, the even and the odd chunks): an issuer hands over the turn after
+    // 20 of its 24 MMAs, so the next chunk's MMAs queue up behind the last
+    // ones without a gap, and the pipeline that has just finished scans its
+    // distances while the tensor core works on the other.  The 24 MMAs of a
+    // chunk are issued straight-line (compile-time operand offsets and
+    // accumulate flags) so that one thread keeps pace with the tensor core.
+    // Each user of a half-chunk commits once to its empty barrier (count 2); a
+    // sole user (a tile alone, or a split chunk) commits twice.  A tile 0
+    // alone takes no turns.
     const int t = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      uint32_t it = 0, builds = 0;
+      uint32_t ch = 0, u = 0, builds = 0;  // chunks gone through, chunks issued, queries
       bool ok = true;
       auto wait_or_fail = [&](uint64_t *b, uint32_t parity) {
         if (ok && !mbar_wait(b, parity)) {
@@ -422,46 +449,49 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       // descriptor of the ring base; an operand adds (byte offset >> 4)
       const uint64_t desc0 = smem_desc(smem_addr(ring), 16, 1024, kSwizzle128B);
       const uint32_t tb = tmem + t * SR_TILE_COLS;
+      const uint32_t ta = SPLIT ? tmem : tb;  // the query's columns
       for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep) {
-        const bool pair = t0 + (int)gridDim.x < n_tiles;  // tile 1 present in this item
-        if (t == 1 && !pair) break;
+        const bool pair = !SPLIT && t0 + (int)gridDim.x < n_tiles;  // tile 1 present in this item
+        if (t == 1 && !pair && !SPLIT) break;
+        const bool turns = SPLIT || pair;
+        const bool twice = !pair;  // sole user of each half-chunk
         for (int q = 0; q < n_q && ok; ++q, ++builds)
-          for (int c = 0; c < nkc && ok; ++c, ++it) {
-            const uint32_t j0 = 2 * it, j1 = j0 + 1;  // the chunk's lo and hi half-chunks
-            const int s0 = j0 % SR_SLOTS, s1 = j1 % SR_SLOTS;
-            if (it > 0 && !wait_or_fail(&bar.acc_empty[t], (it - 1) & 1)) break;
-            if (c == 0 && !wait_or_fail(&bar.a_ready[t], builds & 1)) break;
-            if (!wait_or_fail(&bar.b_full[s0], (j0 / SR_SLOTS) & 1)) break;
-            // turn: tile 1 follows tile 0's chunk `it`; tile 0 follows tile 1's chunk it - 1
-            if (pair && (t == 1 || it > 0) && !wait_or_fail(&bar.turn[t], (t == 1 ? it : it - 1) & 1)) break;
+          for (int c = 0; c < nkc && ok; ++c, ++ch) {
+            if (SPLIT && (c & 1) != t) continue;
+            const uint32_t j0 = 2 * ch, j1 = j0 + 1;  // the chunk's lo and hi half-chunks
+            const int s0 = j0 % SLOTS, s1 = j1 % SLOTS;
+            // the accumulator free, the query built, the lo half in, the turn: issuer
+            // 1's n-th chunk follows issuer 0's n-th, issuer 0's follows issuer 1's (n-1)-th
+            if (u > 0 && !wait_or_fail(&bar.acc_empty[t], (u - 1) & 1)) break;
+            if (c == (SPLIT ? t : 0) && !wait_or_fail(&bar.a_ready[SPLIT ? 0 : t], builds & 1)) break;
+            if (!wait_or_fail(&bar.b_full[s0], (j0 / SLOTS) & 1)) break;
+            if (turns && (t == 1 || u > 0) && !wait_or_fail(&bar.turn[t], (t == 1 ? u : u - 1) & 1)) break;
+            ++u;
             tc_fence_after();
-            const uint64_t bd_lo = desc0 + (uint64_t)((s0 * SR_HALF) >> 4);
-            const uint64_t bd_hi = desc0 + (uint64_t)((s1 * SR_HALF) >> 4);
             // lo half first (a_hi.b_lo, 8 MMAs), then hi (a_hi.b_hi + a_lo.b_hi, 16): the
             // lo half's slot is freed early, and the next chunk's hi half, copied
             // into it, is needed only a third of the way into that chunk
+            const uint64_t bd_lo = desc0 + (uint64_t)((s0 * SR_HALF) >> 4);
 #pragma unroll
-            for (int step = 0; step < 4; ++step) {
-              const bool hi = step >= 2;
-              if (step == 2) {
-                mma_commit(&bar.b_empty[s0]);  // the lo half is free once these MMAs are done
-                if (!pair) mma_commit(&bar.b_empty[s0]);
-                if (!wait_or_fail(&bar.b_full[s1], (j1 / SR_SLOTS) & 1)) break;
-                tc_fence_after();
-              }
-              const uint64_t bd = (hi ? bd_hi : bd_lo) + (uint64_t)(((step & 1) * SR_ATOM) >> 4);
+            for (int m = 0; m < 8; ++m) {
+              const uint64_t b = bd_lo + (uint64_t)((((m >> 2) * SR_ATOM) + (m & 3) * 32) >> 4);
+              mma_tf32_ta(tb + SR_ACC, ta + SR_A_HI + (uint32_t)m * 8, b, SR_IDESC, m == 0 ? 0u : 1u);
+            }
+            mma_commit(&bar.b_empty[s0]);  // the lo half is free once these MMAs are done
+            if (twice) mma_commit(&bar.b_empty[s0]);
+            if (!wait_or_fail(&bar.b_full[s1], (j1 / SLOTS) & 1)) break;
+            tc_fence_after();
+            const uint64_t bd_hi = desc0 + (uint64_t)((s1 * SR_HALF) >> 4);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                if (step == 3 && ks == 2) mbar_arrive(&bar.turn[1 - t]);  // 20 of 24 issued: hand over
-                const uint64_t b = bd + (uint64_t)((ks * 32) >> 4);
-                const uint32_t ka = (uint32_t)((step & 1) * 4 + ks) * 8;
-                mma_tf32_ta(tb + SR_ACC, tb + SR_A_HI + ka, b, SR_IDESC, (step == 0 && ks == 0) ? 0u : 1u);
-                if (hi) mma_tf32_ta(tb + SR_ACC, tb + SR_A_LO + ka, b, SR_IDESC, 1u);
-              }
+            for (int m = 0; m < 8; ++m) {
+              if (m == 6) mbar_arrive(&bar.turn[1 - t]);  // 20 of 24 issued: hand over
+              const uint64_t b = bd_hi + (uint64_t)((((m >> 2) * SR_ATOM) + (m & 3) * 32) >> 4);
+              mma_tf32_ta(tb + SR_ACC, ta + SR_A_HI + (uint32_t)m * 8, b, SR_IDESC, 1u);
+              mma_tf32_ta(tb + SR_ACC, ta + SR_A_LO + (uint32_t)m * 8, b, SR_IDESC, 1u);
             }
             mma_commit(&bar.acc_full[t]);
             mma_commit(&bar.b_empty[s1]);
-            if (!pair) mma_commit(&bar.b_empty[s1]);
+            if (twice) mma_commit(&bar.b_empty[s1]);
           }
       }
       mma_commit(&bar.drain[t]);
@@ -473,9 +503,9 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     const int quarter = warp & 3;      // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem + tile * SR_TILE_COLS + ((uint32_t)(quarter * 32) << 16);
     const int64_t ld = (int64_t)n_q * d;
-    float4 *wpart = reinterpret_cast<float4 *>(smem + SR_RING_BYTES + tile * SR_PART_BYTES) + quarter * 32 * (d / 4);
-    float4 *wstage =
-        reinterpret_cast<float4 *>(smem + SR_RING_BYTES + (2 + tile) * SR_PART_BYTES) + quarter * 32 * (d / 4);
+    unsigned char *tile_area = smem + SR_RING_BYTES + (1 - tile) * 2 * SR_PART_BYTES;
+    float4 *wpart = reinterpret_cast<float4 *>(tile_area) + quarter * 32 * (d / 4);
+    float4 *wstage = reinterpret_cast<float4 *>(tile_area + SR_PART_BYTES) + quarter * 32 * (d / 4);
     const int f0 = lane >> 2, j = lane & 3;       // cooperative layout: frames f0 + 8i, slots 4b + j
     uint64_t *acc_full = &bar.acc_full[tile], *acc_empty = &bar.acc_empty[tile], *a_ready = &bar.a_ready[tile];
     uint32_t cc = 0;
@@ -521,57 +551,93 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       pending = false;
     };
 
-    int my_tile = blockIdx.x + tile * gridDim.x;
-    if (my_tile < n_tiles) {  // the first query's partial: the projection row itself
-      const int64_t n = (int64_t)my_tile * 128 + quarter * 32 + lane;
+    const int n_cta = gridDim.x;
+    // split items: pipeline 1's (value, index) per frame, two column pairs of
+    // its query columns (unused in a split item), in this frame's TMEM lane
+    const uint32_t xch = tmem + SR_TILE_COLS + ((uint32_t)(quarter * 32) << 16) + SR_A_HI;
+    uint32_t ua = 0, xu = 0;  // accumulator uses, stage minima handed over
+    // the first query's partial: the projection row itself (tile 1 only if the first item has one)
+    if (tile == 0 || (!SPLIT && blockIdx.x + n_cta < n_tiles)) {
+      const int64_t n = (int64_t)(blockIdx.x + tile * n_cta) * 128 + quarter * 32 + lane;
       term_issue(P0 + (n < n_rows ? n : 0) * ld, true);
     }
-    for (; my_tile < n_tiles && ok; my_tile += sweep) {
+    for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep) {
+      const bool pair = !SPLIT && t0 + n_cta < n_tiles;
+      constexpr bool split = SPLIT;
+      if (tile == 1 && !pair && !split) break;
+      const bool scan_only = tile == 1 && split;  // half the chunks; no query, no codes
+      const int my_tile = tile == 1 && pair ? t0 + n_cta : t0;
       const int64_t n = (int64_t)my_tile * 128 + quarter * 32 + lane;
       const bool valid = n < n_rows;
       const int64_t n_next = n + (int64_t)sweep * 128;
       const bool has_next = my_tile + sweep < n_tiles;
-      // a tile 0 without a partner tile releases the norm blocks for both
-      const bool alone = tile == 0 && my_tile + (int)gridDim.x >= n_tiles;
+      // a tile 0 without a partner tile or split releases the norm blocks for both
+      const bool alone = !pair && !split;
+      const int n_own = split ? nkc / 2 : nkc;  // chunks scanned per stage
       for (int q = 0; q < n_q && ok; ++q) {
-        // ---- stage boundary: the last term of the query, then the A operand
-        if (pending) term_finish();
-        if (q > 0) {
-          term_issue(G + ((size_t)pair_index(q, q - 1) * K + my_codes[q - 1]) * d, false);
-          term_finish();
-        }
-        __syncwarp();
-        {
-          float p[d];
+        if (!scan_only) {
+          // ---- stage boundary: the query = partial - the last known term (if
+          //      still staged) - the row of the code just found (zero at the
+          //      first stage).  This frame's row of the latter is loaded straight
+          //      into registers (first, so its latency overlaps the wait for the
+          //      staged term), and the query is formed in registers: the
+          //      boundary reads the partial and the staged row once and writes
+          //      no shared memory.  (Subtracting the zero row is exact, and
+          //      keeps one code path.)
+          float4 g[d / 4];
+          const bool has_g = q > 0;
 #pragma unroll
-          for (int u = 0; u < d / 4; ++u) {
-            const float4 t = wpart[lane * (d / 4) + (u ^ (lane & 7))];
-            p[4 * u] = t.x;
-            p[4 * u + 1] = t.y;
-            p[4 * u + 2] = t.z;
-            p[4 * u + 3] = t.w;
+          for (int u = 0; u < d / 4; ++u) g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (has_g) {
+            const float4 *gr =
+                reinterpret_cast<const float4 *>(G + ((size_t)pair_index(q, q - 1) * K + my_codes[q - 1]) * d);
+#pragma unroll
+            for (int u = 0; u < d / 4; ++u) g[u] = __ldg(gr + u);
           }
+          const bool sub_staged = pending && !pending_first;
+          if (pending) {
+            cp_async_wait_all();
+            pending = false;
+          }
+          __syncwarp();  // the warp's copies (this frame's staged row among them) have landed
           // raw (= hi after TF32 truncation) and lo parts into this row's TMEM lane
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float lo[32];
+            float p[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = p[32 * h + i];
-              lo[i] = v - __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+            for (int u = 0; u < 8; ++u) {
+              const int idx = lane * (d / 4) + ((8 * h + u) ^ (lane & 7));
+              float4 t = wpart[idx];
+              if (sub_staged) {
+                const float4 v = wstage[idx];
+                t.x -= v.x;
+                t.y -= v.y;
+                t.z -= v.z;
+                t.w -= v.w;
+              }
+              t.x -= g[8 * h + u].x;
+              t.y -= g[8 * h + u].y;
+              t.z -= g[8 * h + u].z;
+              t.w -= g[8 * h + u].w;
+              p[4 * u] = t.x;
+              p[4 * u + 1] = t.y;
+              p[4 * u + 2] = t.z;
+              p[4 * u + 3] = t.w;
             }
-            tmem_st32(lane_base + SR_A_HI + 32 * h, *reinterpret_cast<const float(*)[32]>(&p[32 * h]));
-            tmem_st32(lane_base + SR_A_LO + 32 * h, lo);
+            tmem_st32(lane_base + SR_A_HI + 32 * h, p);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[i] -= __uint_as_float(__float_as_uint(p[i]) & 0xffffe000u);
+            tmem_st32(lane_base + SR_A_LO + 32 * h, p);
           }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(a_ready);
+          __syncwarp();  // every lane has read its row before the next query's terms overwrite it
         }
-        __syncwarp();  // every lane has read its row before the next query's terms overwrite it
         // ---- terms of the next query known before this stage's code:
         //      next stage: P0[n][q+1], G[q+1][0..q-1];  next tile: P0[n'][0]
         const int q_next = q + 1 < n_q ? q + 1 : 0;
-        const int n_terms = q + 1 < n_q ? q + 1 : (has_next ? 1 : 0);
+        const int n_terms = scan_only ? 0 : q + 1 < n_q ? q + 1 : (has_next ? 1 : 0);
         const int64_t n_row = q + 1 < n_q ? (valid ? n : 0) : (n_next < n_rows ? n_next : 0);
         auto term_row = [&](int t) -> const float * {
           return t == 0 ? P0 + n_row * ld + q_next * d
@@ -582,12 +648,24 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         float best_v = __int_as_float(0x7f800000);
         int best_k = 0;
         for (int c = 0; c < nkc; ++c, ++cc) {
+          const int sn = cc % SR_CN_SLOTS;
+          if (split && (c & 1) != tile) {
+            // the other pipeline's chunk: its norm block is released by both, in order
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar.cn_full[sn], (cc / SR_CN_SLOTS) & 1))) {
+              record_error(status, RVQ_DEVICE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            mbar_arrive(&bar.cn_free[sn]);
+            continue;
+          }
           const int cr = (c + rot) % nkc;
-          if (!__all_sync(0xffffffffu, mbar_wait(acc_full, cc & 1))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(acc_full, (SPLIT ? ua : cc) & 1))) {
             record_error(status, RVQ_DEVICE_TIMEOUT);
             ok = false;
             break;
           }
+          if (SPLIT) ++ua;
           tc_fence_after();
           float v[SR_KC];
 #pragma unroll
@@ -596,7 +674,6 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(acc_empty);  // the accumulator is free: the values are in registers
-          const int sn = cc % SR_CN_SLOTS;
           if (!__all_sync(0xffffffffu, mbar_wait(&bar.cn_full[sn], (cc / SR_CN_SLOTS) & 1))) {
             record_error(status, RVQ_DEVICE_TIMEOUT);
             ok = false;
@@ -635,13 +712,48 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           // ---- this chunk's share of the next query's known terms, in order:
           //      the previous one is added now, the new one stays in flight
           //      until after the next chunk's scan
-          const int target = (n_terms * (c + 1) + nkc - 1) / nkc;
+          const int target = (n_terms * ((split ? c >> 1 : c) + 1) + n_own - 1) / n_own;
           for (; done < target; ++done) {
             if (pending) term_finish();
             term_issue(term_row(done), done == 0);
           }
         }
         if (!ok) break;
+        if (split) {
+          // ---- pipeline 1's minimum of the stage to pipeline 0
+          const uint32_t xb = xch + (xu & 1) * 2;
+          const uint32_t use = xu >> 1;
+          if (scan_only) {
+            if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.xch_free[xu & 1], (use - 1) & 1))) {
+              record_error(status, RVQ_DEVICE_TIMEOUT);
+              ok = false;
+              break;
+            }
+            tmem_st2(xb, __float_as_uint(best_v), (uint32_t)best_k);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.xch_full[xu & 1]);
+            ++xu;
+            continue;
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.xch_full[xu & 1], use & 1))) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t o_v, o_k;
+          tmem_ld2(xb, o_v, o_k);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar.xch_free[xu & 1]);
+          ++xu;
+          const float ov = __uint_as_float(o_v);
+          if (ov < best_v || (ov == best_v && (int)o_k < best_k)) {
+            best_v = ov;
+            best_k = (int)o_k;
+          }
+        }
         my_codes[q] = best_k;
         if (valid) codes[n * n_q + q] = best_k;
       }
@@ -692,7 +804,9 @@ cudaError_t ensure_attributes() {
   if (g_attr_done.load() & bit) return cudaSuccess;
   e = cudaFuncSetAttribute(k_project_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PJ_SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_search_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  e = cudaFuncSetAttribute(k_search_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_search_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
   if (e != cudaSuccess) return e;
   g_attr_done.fetch_or(bit);
   return cudaSuccess;
@@ -736,9 +850,12 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
       tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int tiles = (int)((n + 127) / 128);
-  k_search_tc<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(
-      p0, at<float>(tables, L.g), at<float>(tables, L.cb_img), at<float>(tables, L.cnorm), codes + n0 * n_q, n, n_q,
-      K, tiles, status);
+  // no more tiles than SMs: every item is split, and the ring takes tile 1's areas
+  auto search = tiles <= sms && (K / SR_KC) % 2 == 0 ? k_search_tc<true> : k_search_tc<false>;
+  search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, at<float>(tables, L.g),
+                                                                 at<float>(tables, L.cb_img),
+                                                                 at<float>(tables, L.cnorm), codes + n0 * n_q, n,
+                                                                 n_q, K, tiles, status);
   return cudaGetLastError();
 }
 

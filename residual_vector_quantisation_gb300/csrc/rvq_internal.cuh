@@ -13,6 +13,7 @@ constexpr int kCodeDim = 64;            // d supported by the kernels
 constexpr int kChunkCodes = 128;        // codewords per tensor-core distance chunk
 constexpr size_t kScratchHeader = 256;  // status word at the head of encode scratch
 constexpr int RVQ_DEVICE_TIMEOUT = 5;   // status word value: a bounded device wait gave up
+constexpr int RVQ_DEVICE_BAD_LAUNCH = 6;  // status word value: a kernel refused its launch shape
 constexpr int kMaxStages = 64;         // Q limit
 constexpr size_t kAlign = 256;
 

@@ -185,6 +185,20 @@ def test_other_shapes(D, K, Q):
     run_small(W, x, label=f"D={D} K={K} Q={Q}")
 
 
+@pytest.mark.parametrize("cta_rounds,extra,K", [(1, 37, 256), (3, 11, 512), (1, 37, 384)])
+def test_pair_and_split_items_mixed(cta_rounds, extra, K):
+    """Tile counts just above a multiple of the SM count: some CTAs get a
+    second tile in an item and the rest a lone tile, which is split between
+    the CTA's two pipelines when a stage has an even number of 128-codeword
+    chunks (K = 256, 512) and run by one pipeline otherwise (K = 384).
+    Every frame is checked."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = (cta_rounds * sms + extra) * 128 - 50
+    w, W = _small_weights(D=64, K=K, Q=3, seed=K + extra)
+    x = np.random.default_rng(K).standard_normal((N, 64)).astype(np.float32)
+    run_small(W, x, label=f"tiles={cta_rounds}x{sms}+{extra} K={K}")
+
+
 def test_biases_and_prefix_depths():
     w, W = _small_weights(D=256, K=512, Q=6, bias=True)
     x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
