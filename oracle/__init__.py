@@ -6,8 +6,11 @@ CUDA package, and the CUDA package imports nothing from here.
 
 Functions
 ---------
-encode(weights, x, n_q, threads=0) -> dict(codes, gap, best_dist, residual)
+encode(weights, x, n_q, threads=0, metric="l2") -> dict(codes, gap, best_dist, residual)
     The residual loop of omnivoice.cpp ARCHITECTURE.md, "RVQ codec", in float64.
+    metric="cosine": the quantizer of moss-tts.cpp AGENTS.md, gotcha 9 -- the
+    projection and every codeword are L2-normalised (eps 1e-12) before the
+    argmin; the residual update and decode use the stored codeword.
 decode(weights, codes, n_q, threads=0) -> (y float64 [N][D], n_bad)
     The accumulated decode graph of the same section, in float64.
 reconstruct(weights, x, n_q) -> dict(codes, ..., x_hat)
@@ -54,6 +57,9 @@ def _load():
             f = ctypes.c_void_p
             lib.rvq_oracle_encode.argtypes = [ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int] + [f] * 4 + [ctypes.c_int]
             lib.rvq_oracle_encode.restype = ctypes.c_int
+            lib.rvq_oracle_encode_metric.argtypes = ([ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int]
+                                                     + [f] * 4 + [ctypes.c_int, ctypes.c_int])
+            lib.rvq_oracle_encode_metric.restype = ctypes.c_int
             lib.rvq_oracle_decode.argtypes = [ctypes.c_int] * 4 + [f] * 4 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
             lib.rvq_oracle_decode.restype = ctypes.c_int
             lib.rvq_oracle_version.restype = ctypes.c_char_p
@@ -81,9 +87,13 @@ def _dims(weights):
     return D, d, K, Q
 
 
+METRICS = {"l2": 0, "cosine": 1}
+
+
 def encode(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 0,
-           want_residual: bool = True) -> dict:
+           want_residual: bool = True, metric: str = "l2") -> dict:
     lib = _load()
+    m = METRICS[metric]
     D, d, K, Q = _dims(weights)
     n_q = Q if n_q is None else int(n_q)
     x = _f32(x)
@@ -94,9 +104,14 @@ def encode(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 
     gap = np.empty((N, n_q), dtype=np.float64)
     best = np.empty((N, n_q), dtype=np.float64)
     resid = np.empty((N, D), dtype=np.float64) if want_residual else None
-    rc = lib.rvq_oracle_encode(D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
-                               _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(x), N, n_q, _ptr(codes),
-                               _ptr(gap), _ptr(best), _ptr(resid), int(threads))
+    if m == 0:
+        rc = lib.rvq_oracle_encode(D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
+                                   _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(x), N, n_q, _ptr(codes),
+                                   _ptr(gap), _ptr(best), _ptr(resid), int(threads))
+    else:
+        rc = lib.rvq_oracle_encode_metric(D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
+                                          _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(x), N, n_q, _ptr(codes),
+                                          _ptr(gap), _ptr(best), _ptr(resid), m, int(threads))
     if rc != 0:
         raise ValueError("rvq_oracle_encode rejected its arguments")
     return {"codes": codes, "gap": gap, "best_dist": best, "residual": resid}
@@ -119,8 +134,9 @@ def decode(weights: dict, codes: np.ndarray, n_q: int | None = None, threads: in
     return y, int(n_bad.value)
 
 
-def reconstruct(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 0) -> dict:
-    enc = encode(weights, x, n_q, threads)
+def reconstruct(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 0,
+                metric: str = "l2") -> dict:
+    enc = encode(weights, x, n_q, threads, metric=metric)
     y, _ = decode(weights, enc["codes"], enc["codes"].shape[1], threads)
     enc["x_hat"] = y
     return enc

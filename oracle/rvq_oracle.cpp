@@ -30,6 +30,12 @@
 //     can tell near-ties from clear decisions;
 //   * decode codes outside [0, K) contribute nothing and are counted.
 //
+// The normalised metric (metric 1) is the quantizer of moss-tts.cpp AGENTS.md,
+// gotcha 9: both the projected encoding and every codeword are L2-normalised,
+// v / max(||v||_2, 1e-12), before the argmin; decode stays gather + sum, so
+// the residual update and the decode use the stored codeword itself (the
+// "no extra scaling" of that gotcha is read this way).
+//
 // All arithmetic is float64 (inputs are float32 and widen exactly).  Frames
 // are independent; threads split the frames into contiguous chunks and each
 // frame's arithmetic order is fixed, so the result does not depend on the
@@ -68,8 +74,18 @@ void parallel_frames(int64_t N, int threads, F &&body) {
 
 // One frame of the residual loop.  residual holds x on entry (float64) and
 // the final residual on exit.
-void encode_frame(const Weights &W, int n_q, std::vector<double> &residual, std::vector<double> &e,
-                  int32_t *codes, double *gap, double *best_dist) {
+constexpr double kNormEps = 1e-12;
+
+// v / max(||v||_2, 1e-12), in place.
+void l2_normalise(std::vector<double> &v) {
+  double ss = 0.0;
+  for (double t : v) ss += t * t;
+  const double n = std::max(std::sqrt(ss), kNormEps);
+  for (double &t : v) t /= n;
+}
+
+void encode_frame(const Weights &W, int n_q, int metric, std::vector<double> &residual, std::vector<double> &e,
+                  std::vector<double> &c_n, int32_t *codes, double *gap, double *best_dist) {
   const int D = W.D, d = W.d, K = W.K;
   for (int k = 0; k < n_q; ++k) {
     // e_k = project_in[k](residual)
@@ -82,15 +98,19 @@ void encode_frame(const Weights &W, int n_q, std::vector<double> &residual, std:
       e[j] = s;
     }
     // codes_k = argmin_i || e_k - embed[i] ||^2, lowest index on ties
+    // (metric 1: both sides L2-normalised first)
+    if (metric == 1) l2_normalise(e);
     const float *embed = W.codebook + (size_t)k * K * d;
     int best = -1;
     double d1 = std::numeric_limits<double>::infinity();
     double d2 = std::numeric_limits<double>::infinity();
     for (int i = 0; i < K; ++i) {
       const float *c = embed + (size_t)i * d;
+      for (int j = 0; j < d; ++j) c_n[j] = (double)c[j];
+      if (metric == 1) l2_normalise(c_n);
       double dist = 0.0;
       for (int j = 0; j < d; ++j) {
-        double t = e[j] - (double)c[j];
+        double t = e[j] - c_n[j];
         dist += t * t;
       }
       if (dist < d1) {
@@ -122,29 +142,40 @@ void encode_frame(const Weights &W, int n_q, std::vector<double> &residual, std:
 extern "C" {
 
 // Encode N frames with the first n_q stages.
+//   metric    0: squared L2; 1: squared L2 between L2-normalised vectors
 //   codes     [N][n_q] int32   (required)
 //   gap       [N][n_q] float64 relative gap (d2-d1)/d2 per stage (nullable)
 //   best_dist [N][n_q] float64 best squared distance per stage (nullable)
 //   residual  [N][D]   float64 final residual (nullable)
 // Returns 0 on success, -1 on a bad argument.
-int rvq_oracle_encode(int D, int d, int K, int Q, const float *w_in, const float *b_in,
-                      const float *codebook, const float *w_out, const float *b_out,
-                      const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
-                      double *best_dist, double *residual, int threads) {
+int rvq_oracle_encode_metric(int D, int d, int K, int Q, const float *w_in, const float *b_in,
+                             const float *codebook, const float *w_out, const float *b_out,
+                             const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
+                             double *best_dist, double *residual, int metric, int threads) {
   if (D <= 0 || d <= 0 || K <= 0 || Q <= 0 || N < 0 || n_q < 1 || n_q > Q) return -1;
+  if (metric != 0 && metric != 1) return -1;
   if (!w_in || !codebook || !w_out || (!x && N > 0) || (!codes && N > 0)) return -1;
   Weights W{D, d, K, Q, w_in, b_in, codebook, w_out, b_out};
   parallel_frames(N, threads, [&](int64_t lo, int64_t hi) {
-    std::vector<double> r((size_t)D), e((size_t)d);
+    std::vector<double> r((size_t)D), e((size_t)d), c_n((size_t)d);
     for (int64_t n = lo; n < hi; ++n) {
       for (int i = 0; i < D; ++i) r[i] = (double)x[(size_t)n * D + i];
-      encode_frame(W, n_q, r, e, codes + (size_t)n * n_q, gap ? gap + (size_t)n * n_q : nullptr,
+      encode_frame(W, n_q, metric, r, e, c_n, codes + (size_t)n * n_q, gap ? gap + (size_t)n * n_q : nullptr,
                    best_dist ? best_dist + (size_t)n * n_q : nullptr);
       if (residual)
         for (int i = 0; i < D; ++i) residual[(size_t)n * D + i] = r[i];
     }
   });
   return 0;
+}
+
+// Squared-L2 encode (metric 0).
+int rvq_oracle_encode(int D, int d, int K, int Q, const float *w_in, const float *b_in,
+                      const float *codebook, const float *w_out, const float *b_out,
+                      const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
+                      double *best_dist, double *residual, int threads) {
+  return rvq_oracle_encode_metric(D, d, K, Q, w_in, b_in, codebook, w_out, b_out, x, N, n_q, codes, gap,
+                                  best_dist, residual, 0, threads);
 }
 
 // Decode N frames of codes [N][n_q] into y [N][D] float64:
@@ -186,6 +217,6 @@ int rvq_oracle_decode(int D, int d, int K, int Q, const float *codebook, const f
   return 0;
 }
 
-const char *rvq_oracle_version(void) { return "rvq-oracle f64 1"; }
+const char *rvq_oracle_version(void) { return "rvq-oracle f64 2"; }
 
 }  // extern "C"

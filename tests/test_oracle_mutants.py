@@ -27,6 +27,15 @@ MUTANTS = {
     "second_best_not_tracked": ("} else if (dist < d2) {", "} else if (false) {"),
     "codeword_from_wrong_stage": ("const float *c = embed + (size_t)best * d;",
                                   "const float *c = W.codebook + (size_t)best * d;"),
+    # the normalised metric
+    "cosine_query_not_normalised": ("if (metric == 1) l2_normalise(e);", "(void)0;"),
+    "cosine_codebook_not_normalised": ("if (metric == 1) l2_normalise(c_n);", "(void)0;"),
+    "cosine_eps_added_to_norm": ("std::max(std::sqrt(ss), kNormEps)", "(std::sqrt(ss) + kNormEps)"),
+    "cosine_residual_uses_normalised_codeword": (
+        "for (int j = 0; j < d; ++j) s += (double)row[j] * (double)c[j];\n      if (W.b_out)",
+        "double nn = 0; for (int j = 0; j < d; ++j) nn += (double)c[j] * c[j];\n"
+        "      for (int j = 0; j < d; ++j) s += (double)row[j] * (double)c[j] / (metric == 1 ? std::sqrt(nn) : 1.0);\n"
+        "      if (W.b_out)"),
 }
 
 PINS = [
@@ -42,6 +51,11 @@ PINS = [
     pins.test_decode_scaling_bias_and_prefix,
     pins.test_decode_counts_and_skips_bad_codes,
     pins.test_input_bias_is_a_codebook_shift,
+    pins.test_cosine_closed_form_2d,
+    pins.test_cosine_eps_clamps_small_vectors,
+    pins.test_cosine_single_stage_is_scipy_cosine_neighbour,
+    pins.test_cosine_scale_invariance_of_one_stage,
+    pins.test_cosine_planted_recovery_exact,
 ]
 
 
@@ -61,6 +75,9 @@ def _configure(lib):
     f = ctypes.c_void_p
     lib.rvq_oracle_encode.argtypes = [ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int] + [f] * 4 + [ctypes.c_int]
     lib.rvq_oracle_encode.restype = ctypes.c_int
+    lib.rvq_oracle_encode_metric.argtypes = ([ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int] + [f] * 4
+                                             + [ctypes.c_int, ctypes.c_int])
+    lib.rvq_oracle_encode_metric.restype = ctypes.c_int
     lib.rvq_oracle_decode.argtypes = [ctypes.c_int] * 4 + [f] * 4 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
     lib.rvq_oracle_decode.restype = ctypes.c_int
     lib.rvq_oracle_version.restype = ctypes.c_char_p
@@ -82,7 +99,7 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
 
 
 def test_unmutated_copy_passes_every_pin(tmp_path, monkeypatch):
-    lib = _configure(ctypes.CDLL(_build_mutant(tmp_path, "identity", "rvq-oracle f64 1", "rvq-oracle f64 1")))
+    lib = _configure(ctypes.CDLL(_build_mutant(tmp_path, "identity", "rvq-oracle f64 2", "rvq-oracle f64 2")))
     monkeypatch.setattr(oracle, "_lib", lib)
     for pin in PINS:
         pin()

@@ -319,3 +319,111 @@ def test_rejects_bad_arguments():
         oracle.encode(W, np.zeros((2, 48), np.float32), n_q=6)
     with pytest.raises(ValueError):
         oracle.encode(W, np.zeros((2, 48), np.float32), n_q=0)
+
+
+# ---------------------------------------------------------------------------
+# the normalised ("cosine") metric of moss-tts.cpp AGENTS.md, gotcha 9:
+# projection and codewords L2-normalised (eps 1e-12) before the argmin; the
+# residual update and decode use the stored codeword
+# ---------------------------------------------------------------------------
+
+def _eye_weights(codebook, Q=1):
+    cb = np.asarray(codebook, dtype=np.float64)
+    if cb.ndim == 2:
+        cb = cb[None]
+    Q, K, d = cb.shape
+    eye = np.stack([np.eye(d)] * Q)
+    return _weights(eye, cb, eye)
+
+
+def test_cosine_closed_form_2d():
+    """e = (3, 4) normalises to (0.6, 0.8); the codebook {(1, 0), (0, 2), (0, 0)}
+    normalises to {(1, 0), (0, 1), (0, 0)}.  Squared distances 0.8, 0.4, 1.0:
+    code 1, best distance 0.4, gap (0.8 - 0.4) / 0.8 = 0.5, and the residual
+    subtracts the stored codeword (0, 2), leaving (3, 2)."""
+    W = _eye_weights([[1.0, 0.0], [0.0, 2.0], [0.0, 0.0]])
+    res = oracle.encode(W, np.array([[3.0, 4.0]]), metric="cosine")
+    assert res["codes"].tolist() == [[1]]
+    assert abs(res["best_dist"][0, 0] - 0.4) <= 1e-15
+    assert abs(res["gap"][0, 0] - 0.5) <= 1e-15
+    assert np.array_equal(res["residual"], np.array([[3.0, 2.0]]))
+    # the plain metric on the same frame: distances 20, 13, 25 -> code 1 as
+    # well, best distance 13 (a mix-up of the two metrics shows in best_dist)
+    res0 = oracle.encode(W, np.array([[3.0, 4.0]]))
+    assert res0["codes"].tolist() == [[1]] and res0["best_dist"][0, 0] == 13.0
+
+
+def test_cosine_eps_clamps_small_vectors():
+    """A projection of norm t = 1e-13 < eps is divided by eps, not by its norm:
+    (t, 0) -> (t/eps, 0) ~ (0.1, 0), squared distance to (1, 0) = (1 - t/eps)^2
+    ~ 0.81 and to (0, 1) = (t/eps)^2 + 1; a zero codeword stays zero (distance
+    (t/eps)^2 ~ 0.01).  t is the float32 value the oracle receives."""
+    t = float(np.float32(1e-13))
+    u = t / 1e-12
+    W = _eye_weights([[1.0, 0.0], [0.0, 1.0]])
+    res = oracle.encode(W, np.array([[t, 0.0]]), metric="cosine")
+    assert res["codes"].tolist() == [[0]]
+    assert abs(res["best_dist"][0, 0] - (1.0 - u) ** 2) <= 1e-15
+    assert abs(u - 0.1) < 1e-8
+    W0 = _eye_weights([[1.0, 0.0], [0.0, 0.0]])
+    res = oracle.encode(W0, np.array([[t, 0.0]]), metric="cosine")
+    assert res["codes"].tolist() == [[1]]
+    assert abs(res["best_dist"][0, 0] - u * u) <= 1e-15
+
+
+def test_cosine_single_stage_is_scipy_cosine_neighbour():
+    """One stage with identity projections: the argmin of ||e/|e| - c/|c|||^2
+    = 2 - 2 cos(e, c) is the nearest codeword under scipy's cosine distance,
+    and the best squared distance is twice that distance."""
+    rng = np.random.default_rng(11)
+    d, K, N = 8, 200, 400
+    cb = rng.standard_normal((K, d)).astype(np.float32).astype(np.float64)   # the values the oracle receives
+    x = rng.standard_normal((N, d)).astype(np.float32).astype(np.float64)
+    res = oracle.encode(_eye_weights(cb), x, metric="cosine")
+    cd = cdist(x, cb, metric="cosine")
+    srt = np.sort(cd, axis=1)
+    clear = (srt[:, 1] - srt[:, 0]) > 1e-9
+    assert clear.mean() > 0.99
+    assert np.array_equal(res["codes"][clear, 0], np.argmin(cd, axis=1)[clear])
+    assert np.allclose(res["best_dist"][:, 0], 2.0 * srt[:, 0], rtol=0, atol=1e-12)
+
+
+def test_cosine_scale_invariance_of_one_stage():
+    """With one stage and no input bias, scaling the frames by a positive
+    factor or the codewords by positive factors changes no code."""
+    rng = np.random.default_rng(12)
+    Q, d, D, K, N = 1, 8, 24, 64, 300
+    w_in = rng.standard_normal((Q, d, D)) / np.sqrt(D)
+    w_out = rng.standard_normal((Q, D, d)) / np.sqrt(d)
+    cb = rng.standard_normal((Q, K, d))
+    x = rng.standard_normal((N, D))
+    base = oracle.encode(_weights(w_in, cb, w_out), x, metric="cosine")["codes"]
+    scaled_x = oracle.encode(_weights(w_in, cb, w_out), 8.0 * x, metric="cosine")["codes"]
+    f = np.exp2(rng.integers(-3, 4, size=(Q, K, 1))).astype(np.float64)   # powers of two: exact
+    scaled_cb = oracle.encode(_weights(w_in, cb * f, w_out), x, metric="cosine")["codes"]
+    assert np.array_equal(base, scaled_x)
+    assert np.array_equal(base, scaled_cb)
+    # the plain metric is not scale invariant on the same data
+    assert not np.array_equal(oracle.encode(_weights(w_in, cb * f, w_out), x)["codes"], base)
+
+
+def test_cosine_planted_recovery_exact():
+    """Stages project onto orthogonal 8-d blocks of a 32-d frame; x = sum_q
+    w_out[q] c_q with codewords of varied lengths.  The normalised argmin
+    must return every planted code, the residual (stored codewords
+    subtracted) must vanish, and decode must rebuild x."""
+    rng = np.random.default_rng(13)
+    Q, d, K, N = 4, 8, 32, 200
+    D = Q * d
+    basis = np.linalg.qr(rng.standard_normal((D, D)))[0]
+    w_out = np.stack([basis[:, q * d:(q + 1) * d] for q in range(Q)])       # [Q][D][d]
+    w_in = np.transpose(w_out, (0, 2, 1))                                  # orthonormal: w_in[q] w_out[s] = delta
+    cb = rng.standard_normal((Q, K, d)) * rng.uniform(0.5, 3.0, size=(Q, K, 1))
+    c = rng.integers(0, K, size=(N, Q))
+    x = sum(cb[q, c[:, q]] @ w_out[q].T for q in range(Q))
+    W = _weights(w_in, cb, w_out)
+    res = oracle.encode(W, x, metric="cosine")
+    assert np.array_equal(res["codes"], c)
+    assert np.abs(res["residual"]).max() < 1e-5   # float32 weights: exact up to their rounding
+    y, _ = oracle.decode(W, res["codes"])
+    assert np.abs(y - x).max() < 1e-5
