@@ -19,6 +19,7 @@ the frames are independent and no data-path collective exists).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -141,7 +142,7 @@ def run_reference(args):
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        enc = oracle.encode(W, x, want_residual=False, threads=cores)
+        enc = oracle.encode(W, x, want_residual=False, threads=cores, metric=w.metric)
         oracle.decode(W, enc["codes"], threads=cores)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
@@ -163,7 +164,7 @@ def cpu_baseline_leg(W, x_sample: np.ndarray, w) -> dict:
     import oracle
     cores = os.cpu_count() or 1
     t0 = time.perf_counter()
-    enc = oracle.encode(W, x_sample, want_residual=False, threads=cores)
+    enc = oracle.encode(W, x_sample, want_residual=False, threads=cores, metric=w.metric)
     oracle.decode(W, enc["codes"], threads=cores)
     dt = time.perf_counter() - t0
     return {"value": x_sample.shape[0] / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
@@ -186,13 +187,12 @@ def run_ours(args):
     if w.kind != "planted" and w.kind != "gauss":
         raise SystemExit("bench needs a workload with frames (encode + decode)")
     if args.frames and args.frames < w.N:  # a smaller case of the same workload (profiling)
-        w = ri.Workload(w.name, 1, args.frames, w.D, w.Q, w.K, w.d, w.kind, w.sigma, w.cb_decay, w.seed)
+        w = dataclasses.replace(w, B=1, T=args.frames)
     W = ri.make_weights(w)
     Wt = ri.weights_to_torch(W, dev)
-    rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev)
+    rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev, metric=w.metric)
     # each rank encodes its own batch of the workload's shape: shift the frame seed per rank
-    wr = ri.Workload(w.name, w.B, w.T, w.D, w.Q, w.K, w.d, w.kind, w.sigma, w.cb_decay, w.seed + 1000 * rank) \
-        if rank else w
+    wr = dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
     x = ri.make_x_torch(wr, Wt, dev)
     N, n_q = w.N, w.Q
     codes = torch.empty((N, n_q), dtype=torch.int32, device=dev)
@@ -401,9 +401,9 @@ def per_workload_table(args):
     for w in ri.WORKLOADS:
         W = ri.make_weights(w)
         Wt = ri.weights_to_torch(W, dev)
-        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], device=dev)
+        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], device=dev, metric=w.metric)
         n_q = w.Q
-        row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q}
+        row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q, "K": w.K, "d": w.d, "metric": w.metric}
         if w.kind == "decode":
             codes = torch.from_numpy(ri.make_codes(w)).to(dev)
             x_host = None
@@ -442,7 +442,7 @@ def per_workload_table(args):
             oracle.decode(W, ri.make_codes(w, np.arange(sample)), threads=cores)
         else:
             xs = x[:sample].cpu().numpy()
-            enc = oracle.encode(W, xs, want_residual=False, threads=cores)
+            enc = oracle.encode(W, xs, want_residual=False, threads=cores, metric=w.metric)
             oracle.decode(W, enc["codes"], threads=cores)
         row["oracle_fps"] = sample / (time.perf_counter() - t0)
         row["oracle_cores"] = cores

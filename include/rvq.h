@@ -17,6 +17,11 @@
  *     residual -= w_out[q] . codebook[q][code_q] + b_out[q]
  *   decode:  y = sum_{q < n_q} ( w_out[q] . codebook[q][code_q] + b_out[q] )
  *   with residual = x on entry.
+ * With metric RVQ_METRIC_COSINE the argmin is taken between L2-normalised
+ * vectors, || p_q/n(p_q) - codebook[q][k]/n(codebook[q][k]) ||^2 with
+ * n(v) = max(||v||_2, 1e-12) (moss-tts.cpp AGENTS.md, gotcha 9: the quantizer
+ * L2-normalises the projected encoding and the codebook before the argmin in
+ * code space); the residual update and decode still use the stored codeword.
  *
  * Shapes and layouts (all float32 row-major, PyTorch (out, in) layouts as in
  * that section's tensor table):
@@ -66,8 +71,12 @@ extern "C" {
 #endif
 
 #define RVQ_VERSION_MAJOR 0
-#define RVQ_VERSION_MINOR 1
+#define RVQ_VERSION_MINOR 2
 #define RVQ_VERSION_PATCH 0
+
+/* Distance of the argmin (rvq_dims.metric). */
+#define RVQ_METRIC_L2 0     /* squared L2 between p and the codeword */
+#define RVQ_METRIC_COSINE 1 /* squared L2 between the L2-normalised vectors */
 
 typedef enum rvq_status {
   RVQ_OK = 0,
@@ -79,12 +88,15 @@ typedef enum rvq_status {
 } rvq_status;
 
 /* D: frame (feature) dimension; d: code-space dimension; K: entries per
- * codebook; Q: number of stages held in the tables. */
+ * codebook; Q: number of stages held in the tables; metric: RVQ_METRIC_L2 or
+ * RVQ_METRIC_COSINE (an initialiser that leaves it out gives RVQ_METRIC_L2).
+ * Tables prepared for one metric serve only that metric. */
 typedef struct rvq_dims {
   int32_t D;
   int32_t d;
   int32_t K;
   int32_t Q;
+  int32_t metric;
 } rvq_dims;
 
 /* Device pointers to the per-stage tensors (layouts above). */
@@ -102,9 +114,10 @@ struct CUstream_st;
 typedef struct CUstream_st *rvq_stream_t;
 
 /* RVQ_OK if the kernels handle these dims, else RVQ_ERR_UNSUPPORTED (or
- * RVQ_ERR_INVALID_ARG for non-positive values).  Supported: d == 64,
- * K a multiple of 128 with K <= 65536, D a multiple of 16 with D <= 16384,
- * 1 <= Q <= 64. */
+ * RVQ_ERR_INVALID_ARG for non-positive values or an unknown metric).
+ * Supported: d == 64 with K a multiple of 128, K <= 65536; or d == 8 with K
+ * a multiple of 128, K <= 1024 (two stages' codebooks stay on chip);
+ * D a multiple of 16 with D <= 16384; 1 <= Q <= 64; either metric. */
 RVQ_API rvq_status rvq_dims_supported(rvq_dims dims);
 
 /* Bytes of the tables buffer for these dims (0 if unsupported). */
@@ -112,15 +125,17 @@ RVQ_API size_t rvq_tables_bytes(rvq_dims dims);
 
 /* Fill `tables` (tables_bytes >= rvq_tables_bytes(dims), 256-byte aligned)
  * from the weights.  The tables hold, computed in float64 and rounded once to
- * float32: squared codebook norms; the decode table
+ * float32: squared codebook norms (of the normalised codewords for
+ * RVQ_METRIC_COSINE); the decode table
  *   Z[q][k] = w_out[q] . codebook[q][k] + b_out[q]           ([Q][K][D]);
  * and the cross-stage table
  *   G[q][s][k] = w_in[q] . Z[s][k]   for s < q               ([Q(Q-1)/2][K][d]),
  * which lets encode update every stage's projection without materialising the
  * D-dimensional residual:  w_in[q] . residual_q = w_in[q] . x - sum_{s<q} G[q][s][code_s].
  * Both are exact re-associations of the sums in the "RVQ codec" section.
- * Also a copy of w_in split into TF32 high and low parts, and the codebook in
- * the layouts the kernels read.  Asynchronous on `stream`. */
+ * Also a copy of w_in split into TF32 high and low parts, and -2 x the
+ * codebook (normalised first for RVQ_METRIC_COSINE) split the same way, in the
+ * layouts the kernels read.  Asynchronous on `stream`. */
 RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *tables,
                                size_t tables_bytes, rvq_stream_t stream);
 

@@ -53,8 +53,14 @@ class RVQError(RuntimeError):
         super().__init__(f"{func} returned {STATUS_NAMES.get(status, status)}")
 
 
+RVQ_METRIC_L2 = 0       # include/rvq.h
+RVQ_METRIC_COSINE = 1
+METRICS = {"l2": RVQ_METRIC_L2, "cosine": RVQ_METRIC_COSINE}
+
+
 class rvq_dims(ctypes.Structure):
-    _fields_ = [("D", ctypes.c_int32), ("d", ctypes.c_int32), ("K", ctypes.c_int32), ("Q", ctypes.c_int32)]
+    _fields_ = [("D", ctypes.c_int32), ("d", ctypes.c_int32), ("K", ctypes.c_int32), ("Q", ctypes.c_int32),
+                ("metric", ctypes.c_int32)]
 
 
 class rvq_weights(ctypes.Structure):
@@ -131,8 +137,8 @@ def _check(name: str, status: int):
         raise RVQError(name, status)
 
 
-def _dims(D: int, d: int, K: int, Q: int) -> rvq_dims:
-    return rvq_dims(int(D), int(d), int(K), int(Q))
+def _dims(D: int, d: int, K: int, Q: int, metric: int = RVQ_METRIC_L2) -> rvq_dims:
+    return rvq_dims(int(D), int(d), int(K), int(Q), int(metric))
 
 
 def rvq_dims_supported(dims: rvq_dims) -> int:
@@ -231,9 +237,12 @@ class RVQ:
 
     w_in [Q][d][D], codebook [Q][K][d], w_out [Q][D][d], b_in [Q][d] or None,
     b_out [Q][D] or None; float32 tensors (moved to `device` if needed).
+    metric: "l2" (squared L2) or "cosine" (both sides L2-normalised before the
+    argmin, as RVQ_METRIC_COSINE in include/rvq.h).
     """
 
-    def __init__(self, w_in, codebook, w_out, b_in=None, b_out=None, device=None, stream=None):
+    def __init__(self, w_in, codebook, w_out, b_in=None, b_out=None, device=None, stream=None,
+                 metric: str = "l2"):
         device = torch.device(device) if device is not None else (w_in.device if w_in.is_cuda else torch.device("cuda"))
         f = lambda t: None if t is None else t.to(device=device, dtype=torch.float32).contiguous()
         w_in, codebook, w_out, b_in, b_out = map(f, (w_in, codebook, w_out, b_in, b_out))
@@ -241,7 +250,8 @@ class RVQ:
         K = codebook.shape[1]
         self.D, self.d, self.K, self.Q = D, d, K, Q
         self.device = device
-        self.dims = _dims(D, d, K, Q)
+        self.metric = metric
+        self.dims = _dims(D, d, K, Q, METRICS[metric])
         status = rvq_dims_supported(self.dims)
         _check("rvq_dims_supported", status)
         nbytes = rvq_tables_bytes(self.dims)

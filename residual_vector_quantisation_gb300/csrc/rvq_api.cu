@@ -20,8 +20,9 @@ bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) 
 
 rvq_status check_dims(const rvq_dims &dm) {
   if (dm.D <= 0 || dm.d <= 0 || dm.K <= 0 || dm.Q <= 0) return RVQ_ERR_INVALID_ARG;
-  if (dm.d != rvq::kCodeDim) return RVQ_ERR_UNSUPPORTED;
-  if (dm.K % 128 != 0 || dm.K > 65536) return RVQ_ERR_UNSUPPORTED;
+  if (dm.metric != RVQ_METRIC_L2 && dm.metric != RVQ_METRIC_COSINE) return RVQ_ERR_INVALID_ARG;
+  if (dm.d != rvq::kCodeDim && dm.d != rvq::kCodeDimSmall) return RVQ_ERR_UNSUPPORTED;
+  if (dm.K % 128 != 0 || dm.K > (dm.d == rvq::kCodeDim ? 65536 : rvq::kMaxKSmall)) return RVQ_ERR_UNSUPPORTED;
   if (dm.D % 16 != 0 || dm.D > 16384) return RVQ_ERR_UNSUPPORTED;
   if (dm.Q > rvq::kMaxStages) return RVQ_ERR_UNSUPPORTED;
   return RVQ_OK;
@@ -161,6 +162,6 @@ RVQ_API const char *rvq_status_string(rvq_status status) {
   return "unknown status";
 }
 
-RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.1.0 (sm_103a)"; }
+RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.2.0 (sm_103a)"; }
 
 }  // extern "C"

@@ -224,12 +224,16 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
           tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + t * 256 + c, v);
           tmem_wait_ld();
           if (n < n_rows && c0 + c < n_cols) {
+            // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
+            const int n4 = min(8, (n_cols - (c0 + c)) / 4);
             const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0 + c);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const float4 b = __ldg(b4 + u);
-              reinterpret_cast<float4 *>(out + c)[u] =
-                  make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
+              if (u < n4) {
+                const float4 b = __ldg(b4 + u);
+                reinterpret_cast<float4 *>(out + c)[u] =
+                    make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
+              }
             }
           }
         }
@@ -322,7 +326,7 @@ template <bool SPLIT>
 __global__ void __launch_bounds__(SR_THREADS, 1)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
-                int n_tiles, int *__restrict__ status) {
+                int n_tiles, int metric, int *__restrict__ status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -555,7 +559,8 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     // split items: pipeline 1's (value, index) per frame, two column pairs of
     // its query columns (unused in a split item), in this frame's TMEM lane
     const uint32_t xch = tmem + SR_TILE_COLS + ((uint32_t)(quarter * 32) << 16) + SR_A_HI;
-    uint32_t ua = 0, xu = 0;  // accumulator uses, stage minima handed over
+    uint32_t ua = 0, xu = 0, nb = 0;  // accumulator uses, stage minima handed over, queries seen
+    float s_row = 1.0f;               // this frame's distance scale (1 / n(p) for the cosine metric)
     // the first query's partial: the projection row itself (tile 1 only if the first item has one)
     if (tile == 0 || (!SPLIT && blockIdx.x + n_cta < n_tiles)) {
       const int64_t n = (int64_t)(blockIdx.x + tile * n_cta) * 128 + quarter * 32 + lane;
@@ -601,6 +606,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           }
           __syncwarp();  // the warp's copies (this frame's staged row among them) have landed
           // raw (= hi after TF32 truncation) and lo parts into this row's TMEM lane
+          float ss = 0.0f;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float p[32];
@@ -626,13 +632,32 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             }
             tmem_st32(lane_base + SR_A_HI + 32 * h, p);
 #pragma unroll
+            for (int i = 0; i < 32; ++i) ss = fmaf(p[i], p[i], ss);
+#pragma unroll
             for (int i = 0; i < 32; ++i) p[i] -= __uint_as_float(__float_as_uint(p[i]) & 0xffffe000u);
             tmem_st32(lane_base + SR_A_LO + 32 * h, p);
           }
+          // cosine metric: the query stays raw in TMEM and its distances are
+          // scaled by 1 / max(||p||, 1e-12) in the scan
+          s_row = metric == RVQ_METRIC_COSINE ? 1.0f / fmaxf(sqrtf(ss), 1e-12f) : 1.0f;
+          if (split) tmem_st2(xch + 4, __float_as_uint(s_row), 0u);  // for pipeline 1
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(a_ready);
           __syncwarp();  // every lane has read its row before the next query's terms overwrite it
+        } else {
+          // pipeline 1 of a split item: this stage's query is built; its distance scale
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar.a_ready[0], nb & 1))) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          ++nb;
+          tc_fence_after();
+          uint32_t sv, unused;
+          tmem_ld2(xch + 4, sv, unused);
+          tmem_wait_ld();
+          s_row = __uint_as_float(sv);
         }
         // ---- terms of the next query known before this stage's code:
         //      next stage: P0[n][q+1], G[q+1][0..q-1];  next tile: P0[n'][0]
@@ -679,23 +704,16 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             ok = false;
             break;
           }
+          // distance (up to this frame's constant): s * (-2 p.c) + ||c||^2, with
+          // s = 1 for the plain metric (exact) and 1 / n(p) for the cosine one
           const float4 *cn4 = reinterpret_cast<const float4 *>(cn_buf + sn * SR_KC);
 #pragma unroll
           for (int u = 0; u < SR_KC / 4; ++u) {
             const float4 cn = cn4[u];
-            v[4 * u] += cn.x;
-            v[4 * u + 1] += cn.y;
-            v[4 * u + 2] += cn.z;
-            v[4 * u + 3] += cn.w;
+            fma2(v[4 * u], v[4 * u + 1], s_row, cn.x, cn.y);
+            fma2(v[4 * u + 2], v[4 * u + 3], s_row, cn.z, cn.w);
           }
-          float mm[SR_KC / 2];
-#pragma unroll
-          for (int i = 0; i < SR_KC / 2; ++i) mm[i] = fminf(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-          for (int w2 = SR_KC / 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-            for (int i = 0; i < w2; ++i) mm[i] = fminf(mm[i], mm[i + w2]);
-          const float m = mm[0];
+          const float m = min128(v);
           mbar_arrive(&bar.cn_free[sn]);  // the norms are in registers
           if (alone) mbar_arrive(&bar.cn_free[sn]);
           if (m <= best_v) {  // rare after the first chunks: locate the first index holding m
@@ -849,13 +867,15 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   k_project_tc<<<items1 < sms ? items1 : sms, PJ_THREADS, PJ_SMEM, st>>>(
       tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (d == kCodeDimSmall)
+    return launch_search8(dm, tables, p0, n, n_q, codes + n0 * n_q, status, sms, st);
   const int tiles = (int)((n + 127) / 128);
   // no more tiles than SMs: every item is split, and the ring takes tile 1's areas
   auto search = tiles <= sms && (K / SR_KC) % 2 == 0 ? k_search_tc<true> : k_search_tc<false>;
   search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, at<float>(tables, L.g),
                                                                  at<float>(tables, L.cb_img),
                                                                  at<float>(tables, L.cnorm), codes + n0 * n_q, n,
-                                                                 n_q, K, tiles, status);
+                                                                 n_q, K, tiles, dm.metric, status);
   return cudaGetLastError();
 }
 

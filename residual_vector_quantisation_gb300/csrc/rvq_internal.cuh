@@ -9,7 +9,9 @@
 
 namespace rvq {
 
-constexpr int kCodeDim = 64;            // d supported by the kernels
+constexpr int kCodeDim = 64;            // d of the main kernels
+constexpr int kCodeDimSmall = 8;        // d of the small-code-space kernels
+constexpr int kMaxKSmall = 1024;        // K limit at d = 8 (two stages' codebooks on chip)
 constexpr int kChunkCodes = 128;        // codewords per tensor-core distance chunk
 constexpr size_t kScratchHeader = 256;  // status word at the head of encode scratch
 constexpr int RVQ_DEVICE_TIMEOUT = 5;   // status word value: a bounded device wait gave up
@@ -67,6 +69,8 @@ inline const T *at(const void *base, size_t off) {
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t s);
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0,
                                 int64_t n, int n_q, int32_t *codes, float *p0, int *status, cudaStream_t s);
+cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q,
+                           int32_t *codes, int *status, int sms, cudaStream_t s);
 cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t *codes, int64_t n,
                           int n_q, float *y, int64_t *bad, cudaStream_t s);
 

@@ -4,7 +4,8 @@
 // entry is the correctly rounded value of its exact-arithmetic definition up
 // to float64 summation error (about 1e-16 relative).
 //
-//   cnorm[q][k]   = ||codebook[q][k]||^2
+//   cnorm[q][k]   = ||codebook[q][k]||^2        (cosine metric: ||c / n(c)||^2,
+//                                               n(c) = max(||c||_2, 1e-12))
 //   Z[q][k]       = w_out[q] . codebook[q][k] + b_out[q]         (decode table)
 //   G[q][s][k]    = w_in[q] . Z[s][k]            for s < q      (cross-stage table)
 //
@@ -37,20 +38,35 @@ __global__ void k_prep_w_in(const float *__restrict__ w_in, const float *__restr
   for (int64_t e = i; e < nb; e += stride) b_in_copy[e] = b_in ? b_in[e] : 0.0f;
 }
 
-// Squared codebook norms (float64 sums).
-__global__ void k_prep_cnorm(const float *__restrict__ cb, float *__restrict__ cnorm, int d, int64_t n_rows) {
+// n(c) = max(||c||_2, 1e-12) of one codeword (float64), the divisor of the
+// cosine metric (moss-tts.cpp AGENTS.md, gotcha 9); 1 for the plain metric.
+__device__ __forceinline__ double codeword_divisor(const float *c, int d, int metric) {
+  if (metric != RVQ_METRIC_COSINE) return 1.0;
+  double s = 0.0;
+  for (int j = 0; j < d; ++j) s += (double)c[j] * (double)c[j];
+  return fmax(sqrt(s), 1e-12);
+}
+
+// Squared norms of the codewords as the distance uses them (float64 sums).
+__global__ void k_prep_cnorm(const float *__restrict__ cb, float *__restrict__ cnorm, int d, int64_t n_rows,
+                             int metric) {
   int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // row = q*K + k
   if (r >= n_rows) return;
   const float *src = cb + r * d;
+  const double nrm = codeword_divisor(src, d, metric);
   double s = 0.0;
-  for (int j = 0; j < d; ++j) s += (double)src[j] * (double)src[j];
+  for (int j = 0; j < d; ++j) {
+    const double v = (double)src[j] / nrm;
+    s += v * v;
+  }
   cnorm[r] = (float)s;
 }
 
-// -2 * codebook in TF32 hi/lo halves, laid out as the shared-memory image the
-// tensor-core search loads with one bulk copy per half chunk:
+// -2 * codebook (each codeword divided by n(c) first for the cosine metric)
+// in TF32 hi/lo halves, laid out as the shared-memory image the tensor-core
+// search loads with one bulk copy per half chunk:
 // [q][chunk of 128][hi, lo][atom j/32][sw128(row = k % 128, j % 32)].
-__global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ img, int K, int64_t n) {
+__global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ img, int K, int64_t n, int metric) {
   constexpr int d = kCodeDim;
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*K*d
   if (e >= n) return;
@@ -58,7 +74,7 @@ __global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ 
   const int64_t qk = e / d;
   const int q = (int)(qk / K), k = (int)(qk % K);
   const int c = k / kChunkCodes, kk = k % kChunkCodes;
-  const float v = -2.0f * cb[e];
+  const float v = (float)(-2.0 * (double)cb[e] / codeword_divisor(cb + qk * d, d, metric));
   const float hi = tf32_trunc(v);
   const float lo = v - hi;
   const int64_t chunk = ((int64_t)q * (K / kChunkCodes) + c) * 2;
@@ -67,13 +83,33 @@ __global__ void k_prep_cb_img(const float *__restrict__ cb, float *__restrict__ 
   img[(chunk + 1) * (2 * 128 * 32) + off] = lo;
 }
 
+// The same for d = 8: [q][chunk of 128][hi, lo][sw32(row = k % 128, j)], a
+// 4 KB block per half; a stage's chunks are contiguous, so one bulk copy
+// brings a whole stage.
+__global__ void k_prep_cb_img8(const float *__restrict__ cb, float *__restrict__ img, int K, int64_t n, int metric) {
+  constexpr int d = kCodeDimSmall;
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*K*d
+  if (e >= n) return;
+  const int j = (int)(e % d);
+  const int64_t qk = e / d;
+  const int q = (int)(qk / K), k = (int)(qk % K);
+  const int c = k / kChunkCodes, kk = k % kChunkCodes;
+  const float v = (float)(-2.0 * (double)cb[e] / codeword_divisor(cb + qk * d, d, metric));
+  const float hi = tf32_trunc(v);
+  const float lo = v - hi;
+  const int64_t chunk = ((int64_t)q * (K / kChunkCodes) + c) * 2;
+  const uint32_t off = ptx::sw32_offset(kk, j) / 4;
+  img[(chunk + 0) * (128 * d) + off] = hi;
+  img[(chunk + 1) * (128 * d) + off] = lo;
+}
+
 // Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64).
 // grid: (ceil(D/256), Q*K/16); each block handles 16 codewords of one stage.
+template <int d>
 __global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
                                                 const float *__restrict__ b_out,
                                                 const float *__restrict__ cb, float *__restrict__ z,
                                                 int D, int K) {
-  constexpr int d = kCodeDim;
   __shared__ double sc[16][d];
   const int64_t row0 = (int64_t)blockIdx.y * 16;  // q*K + k0
   const int q = (int)(row0 / K);
@@ -96,24 +132,27 @@ __global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
 }
 
 // M[t][j][m] = sum_i w_in[q][j][i] w_out[s][i][m];  vb[t][j] = sum_i w_in[q][j][i] b_out[s][i].
-// grid: (P, d); block: d threads (one per m) plus one warp for vb.
+// grid: (P, d); block: d threads (one per m), rounded up to whole warps, plus
+// one warp for vb.
+template <int d>
 __global__ void k_prep_m(const float *__restrict__ w_in, const float *__restrict__ w_out,
                          const float *__restrict__ b_out, double *__restrict__ m64,
                          double *__restrict__ vb64, int D, int Q) {
-  constexpr int d = kCodeDim;
   const int t = blockIdx.x, j = blockIdx.y;
   int q = 1;
   while ((int64_t)(q + 1) * q / 2 <= t) ++q;  // t = q(q-1)/2 + s
   const int s = t - q * (q - 1) / 2;
   const float *wi = w_in + ((int64_t)q * d + j) * D;
-  if (threadIdx.x < d) {
+  constexpr int kMThreads = (d + 31) / 32 * 32;
+  if (threadIdx.x < kMThreads) {
     const int m = threadIdx.x;
+    if (m >= d) return;
     const float *wo = w_out + (int64_t)s * D * d + m;
     double acc = 0.0;
     for (int i = 0; i < D; ++i) acc += (double)wi[i] * (double)wo[(int64_t)i * d];
     m64[((int64_t)t * d + j) * d + m] = acc;
   } else {
-    const int lane = threadIdx.x - d;  // one warp
+    const int lane = threadIdx.x - kMThreads;  // one whole warp
     double acc = 0.0;
     if (b_out)
       for (int i = lane; i < D; i += 32) acc += (double)wi[i] * (double)b_out[(int64_t)s * D + i];
@@ -124,12 +163,12 @@ __global__ void k_prep_m(const float *__restrict__ w_in, const float *__restrict
 }
 
 // G[t][k][j] = sum_m M[t][j][m] codebook[s][k][m] + vb[t][j]   (f64 -> f32).
-// grid: (P, K/16); 256 threads = 16 codewords x 16 groups of 4 j.
+// grid: (P, K/16); 256 threads = 16 codewords x 16 groups of d/16 j.
+template <int d>
 __global__ void __launch_bounds__(256) k_prep_g(const double *__restrict__ m64,
                                                 const double *__restrict__ vb64,
                                                 const float *__restrict__ cb, float *__restrict__ g,
                                                 int K) {
-  constexpr int d = kCodeDim;
   __shared__ double sm[d][d + 1];
   __shared__ double sc[16][d];
   const int t = blockIdx.x;
@@ -142,8 +181,9 @@ __global__ void __launch_bounds__(256) k_prep_g(const double *__restrict__ m64,
     sc[e / d][e % d] = (double)cb[(((int64_t)s * K) + k0 + e / d) * d + e % d];
   __syncthreads();
   const int kk = threadIdx.x / 16, jg = threadIdx.x % 16;
-  for (int u = 0; u < 4; ++u) {
-    const int j = jg * 4 + u;
+  for (int u = 0; u < (d + 15) / 16; ++u) {
+    const int j = jg * ((d + 15) / 16) + u;
+    if (j >= d) break;
     double acc = vb64[(int64_t)t * d + j];
     for (int m = 0; m < d; ++m) acc += sm[j][m] * sc[kk][m];
     g[(((int64_t)t * K) + k0 + kk) * d + j] = (float)acc;
@@ -152,23 +192,39 @@ __global__ void __launch_bounds__(256) k_prep_g(const double *__restrict__ m64,
 
 }  // namespace
 
+template <int d>
+void launch_tables(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t st) {
+  const TablesLayout L = tables_layout(dm);
+  const int D = dm.D, K = dm.K, Q = dm.Q;
+  const int64_t rows = (int64_t)Q * K, P = n_pairs(Q);
+  k_prep_z<d><<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
+                                                                             at<float>(tables, L.z), D, K);
+  if (P > 0) {
+    k_prep_m<d><<<dim3((unsigned)P, d), (d + 31) / 32 * 32 + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
+                                                         at<double>(tables, L.vb64), D, Q);
+    k_prep_g<d><<<dim3((unsigned)P, K / 16), 256, 0, st>>>(at<double>(tables, L.m64), at<double>(tables, L.vb64),
+                                                           w.codebook, at<float>(tables, L.g), K);
+  }
+}
+
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t st) {
   const TablesLayout L = tables_layout(dm);
   const int D = dm.D, d = dm.d, K = dm.K, Q = dm.Q;
-  const int64_t nw = (int64_t)Q * d * D, P = n_pairs(Q);
+  const int64_t nw = (int64_t)Q * d * D;
   k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
                                    at<float>(tables, L.b_in), nw, (int64_t)Q * d);
   const int64_t rows = (int64_t)Q * K;
-  k_prep_cnorm<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cnorm), d, rows);
+  k_prep_cnorm<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cnorm), d, rows,
+                                                               dm.metric);
   const int64_t ncb = (int64_t)Q * K * d;
-  k_prep_cb_img<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb);
-  k_prep_z<<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
-                                                                          at<float>(tables, L.z), D, K);
-  if (P > 0) {
-    k_prep_m<<<dim3((unsigned)P, d), d + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
-                                                      at<double>(tables, L.vb64), D, Q);
-    k_prep_g<<<dim3((unsigned)P, K / 16), 256, 0, st>>>(at<double>(tables, L.m64), at<double>(tables, L.vb64),
-                                                        w.codebook, at<float>(tables, L.g), K);
+  if (d == kCodeDim) {
+    k_prep_cb_img<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb,
+                                                                 dm.metric);
+    launch_tables<kCodeDim>(dm, w, tables, st);
+  } else {
+    k_prep_cb_img8<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb,
+                                                                  dm.metric);
+    launch_tables<kCodeDimSmall>(dm, w, tables, st);
   }
   return cudaGetLastError();
 }

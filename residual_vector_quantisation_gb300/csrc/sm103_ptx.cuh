@@ -129,6 +129,11 @@ __device__ __forceinline__ float4 ld_once(const float4 *p) {
 __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem) : "memory");
 }
+// The same through L1 (16 bytes, L1-allocating): a second copy from the same
+// 32-byte sector hits L1.
+__device__ __forceinline__ void cp_async16_ca(void *dst_smem, const void *src_gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
@@ -239,12 +244,58 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
 // 32 lanes x 32 bits, 2 consecutive columns per thread.
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
 }
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t &a, uint32_t &b) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr));
+}
+
+// ---------------------------------------------------------------------------
+// packed and three-input float arithmetic (sm_100 family)
+// ---------------------------------------------------------------------------
+// min(a, b, c) in one instruction.
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0, x1) = (x0 * s + c0, x1 * s + c1), two round-to-nearest FMAs in one
+// instruction (each exactly as fmaf would round it).
+__device__ __forceinline__ void fma2(float &x0, float &x1, float s, float c0, float c1) {
+  unsigned long long a, b, c, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(d));
+}
+
+// Minimum of 128 values by a tree of three-input minima (66 instructions).
+__device__ __forceinline__ float min128(const float (&v)[128]) {
+  float a[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) a[i] = fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[42] = fminf(v[126], v[127]);
+  float b[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = fmin3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = a[42];
+  float c[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) c[i] = fmin3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return fminf(fmin3(c[0], c[1], c[2]), fminf(c[3], c[4]));
 }
 
 // ---------------------------------------------------------------------------
@@ -285,6 +336,13 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t k) {
 // of a TMA load with CU_TENSOR_MAP_SWIZZLE_64B.
 __host__ __device__ constexpr uint32_t sw64_offset(uint32_t row, uint32_t k) {
   return (row >> 3) * 512u + (row & 7u) * 64u + ((((k >> 2) ^ ((row & 7u) >> 1)) & 3u) << 4) + (k & 3u) * 4u;
+}
+
+// Byte offset of element (row, k) of a K-major fp32 tile stored in 32-byte
+// swizzled atoms (8 rows x 8 elements; 8-row groups 256 B apart): the layout
+// a descriptor with 32-byte swizzling reads.
+__host__ __device__ constexpr uint32_t sw32_offset(uint32_t row, uint32_t k) {
+  return (row >> 3) * 256u + (row & 7u) * 32u + ((((k >> 2) ^ ((row & 7u) >> 2)) & 1u) << 4) + (k & 3u) * 4u;
 }
 
 }  // namespace ptx

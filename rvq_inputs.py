@@ -26,7 +26,7 @@ Gaussians are formed in float64 and rounded once to float32.
 
 Workloads
 ---------
-The five workloads are the RVQ shapes of the OmniVoice codec (8 stages,
+The workloads are the RVQ shapes of the OmniVoice codec (8 stages,
 1024 entries of dimension 64 at 25 Hz; omnivoice.cpp ARCHITECTURE.md, sections
 "GGUF layout" and "RVQ codec") and of the MOSS audio tokenizer (32 stages at
 12.5 Hz; moss-tts.cpp AGENTS.md, "What this project is").  Weights follow the
@@ -77,6 +77,7 @@ class Workload:
     sigma: float = 0.0   # planted noise standard deviation
     cb_decay: float = 1.0
     seed: int = BASE_SEED
+    metric: str = "l2"   # "l2" | "cosine" (argmin between L2-normalised vectors)
 
     @property
     def N(self) -> int:
@@ -85,7 +86,7 @@ class Workload:
     def describe(self) -> str:
         return (f"{self.name}: B={self.B} T={self.T} N={self.N} D={self.D} Q={self.Q} "
                 f"K={self.K} d={self.d} kind={self.kind} sigma={self.sigma} "
-                f"cb_decay={self.cb_decay} seed={self.seed}")
+                f"cb_decay={self.cb_decay} seed={self.seed} metric={self.metric}")
 
 
 WORKLOADS = [
@@ -97,6 +98,10 @@ WORKLOADS = [
     # ten books of 4096 entries (the pages' Audio8 codec); the latent sizes D, d
     # are not given there, so D=1024, d=64 as in the other shapes
     Workload("k4096_q10", 16, 750, 1024, 10, 4096, 64, "planted", sigma=0.05, seed=BASE_SEED + 5),
+    # the MOSS tokenizer's quantizer: 32 books of 1024 entries, argmin between
+    # L2-normalised vectors in an 8-dim code space (moss-tts.cpp AGENTS.md,
+    # gotchas 9 and 12); the latent size is not given there, D=768 as moss_deep
+    Workload("moss_lfq", 32, 375, 768, 32, 1024, 8, "gauss", cb_decay=0.8, seed=BASE_SEED + 6, metric="cosine"),
 ]
 WORKLOAD_BY_NAME = {w.name: w for w in WORKLOADS}
 

@@ -20,6 +20,8 @@ int main(void) {
   rvq_dims ok = {1024, 64, 1024, 8};
   rvq_dims bad_d = {1024, 32, 1024, 8};
   rvq_dims zero = {0, 64, 1024, 8};
+  rvq_dims lfq = {768, 8, 1024, 32, RVQ_METRIC_COSINE};
+  rvq_dims bad_metric = {1024, 64, 1024, 8, 7};
   rvq_weights w;
   int32_t fake_codes[4];
   memset(&w, 0, sizeof w);
@@ -27,6 +29,8 @@ int main(void) {
   EXPECT(rvq_dims_supported(ok) == RVQ_OK);
   EXPECT(rvq_dims_supported(bad_d) == RVQ_ERR_UNSUPPORTED);
   EXPECT(rvq_dims_supported(zero) == RVQ_ERR_INVALID_ARG);
+  EXPECT(rvq_dims_supported(lfq) == RVQ_OK);
+  EXPECT(rvq_dims_supported(bad_metric) == RVQ_ERR_INVALID_ARG);
   EXPECT(rvq_tables_bytes(ok) > 0);
   EXPECT(rvq_tables_bytes(bad_d) == 0);
   EXPECT(rvq_encode_scratch_bytes(ok, 1000, 8) >= rvq_encode_min_scratch_bytes(ok, 8));

@@ -50,6 +50,13 @@ def test_early_return_paths(lib_path):
     assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1000, 8)) == -2   # K % 128
     assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 65)) == -2  # Q > 64
     assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, -1, 8)) == -1
+    # the 8-dim code space (K <= 1024) and the normalised metric
+    assert lib.rvq_dims_supported(rq.rvq_dims(768, 8, 1024, 32, rq.RVQ_METRIC_COSINE)) == 0
+    assert lib.rvq_dims_supported(rq.rvq_dims(768, 8, 1024, 32, rq.RVQ_METRIC_L2)) == 0
+    assert lib.rvq_dims_supported(rq.rvq_dims(768, 8, 2048, 32)) == -2   # K too large for d = 8
+    assert lib.rvq_dims_supported(rq.rvq_dims(768, 16, 1024, 32)) == -2  # d neither 8 nor 64
+    assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 8, 2)) == -1  # unknown metric
+    assert lib.rvq_tables_bytes(rq.rvq_dims(768, 8, 1024, 32, 1)) > 0
     assert lib.rvq_tables_bytes(ok) > 8 * 1024 * 1024 * 4                # holds Z at least
     assert lib.rvq_encode_min_scratch_bytes(ok, 8) == 256 + 128 * 8 * 64 * 4
     assert lib.rvq_encode_scratch_bytes(ok, 100, 8) == 256 + 100 * 8 * 64 * 4

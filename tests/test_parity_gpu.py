@@ -32,16 +32,16 @@ def _lib():
     rq.load_library()
 
 
-def make_rvq(W):
+def make_rvq(W, metric="l2"):
     t = ri.weights_to_torch(W, DEV)
-    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV)
+    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV, metric=metric)
 
 
-def check_encode(W, x, codes_gpu, rows=None, n_q=None, x_rms=None, x_hat_gpu=None, label=""):
+def check_encode(W, x, codes_gpu, rows=None, n_q=None, x_rms=None, x_hat_gpu=None, label="", metric="l2"):
     """Oracle-encode x[rows]; compare codes (near-tie rule) and x_hat."""
     rows = np.arange(x.shape[0]) if rows is None else rows
     xs = x[rows]
-    ref = oracle.encode(W, xs, n_q, want_residual=False)
+    ref = oracle.encode(W, xs, n_q, want_residual=False, metric=metric)
     cg = codes_gpu[rows]
     res = compare_codes(cg, ref["codes"], ref["gap"])
     assert res["n_fail"] == 0, f"{label}: code mismatches at clear decisions: {res}"
@@ -54,15 +54,15 @@ def check_encode(W, x, codes_gpu, rows=None, n_q=None, x_rms=None, x_hat_gpu=Non
     return res
 
 
-def run_small(W, x, n_q=None, label=""):
-    rvq = make_rvq(W)
+def run_small(W, x, n_q=None, label="", metric="l2"):
+    rvq = make_rvq(W, metric)
     xt = torch.from_numpy(x).to(DEV)
     codes, x_hat = rvq.reconstruct(xt, n_q)
     codes_e = rvq.encode(xt, n_q)
     torch.cuda.synchronize()
     c = codes.cpu().numpy()
     assert np.array_equal(c, codes_e.cpu().numpy()), "encode and reconstruct disagree"
-    res = check_encode(W, x, c, n_q=n_q, x_hat_gpu=x_hat.cpu().numpy(), label=label)
+    res = check_encode(W, x, c, n_q=n_q, x_hat_gpu=x_hat.cpu().numpy(), label=label, metric=metric)
     # decode through the decode entry point too
     y = rvq.decode(codes).cpu().numpy()
     assert np.array_equal(y, x_hat.cpu().numpy())
@@ -165,8 +165,8 @@ def test_large_batch_workload_full_size_sampled():
 # edge cases
 # ---------------------------------------------------------------------------
 
-def _small_weights(D=64, K=256, Q=4, seed=3, bias=False, decay=1.0):
-    w = ri.Workload("edge", 1, 1, D, Q, K, 64, "gauss", cb_decay=decay, seed=seed)
+def _small_weights(D=64, K=256, Q=4, seed=3, bias=False, decay=1.0, d=64):
+    w = ri.Workload("edge", 1, 1, D, Q, K, d, "gauss", cb_decay=decay, seed=seed)
     return w, ri.make_weights(w, with_bias=bias, bias_scale=0.3)
 
 
@@ -185,8 +185,9 @@ def test_other_shapes(D, K, Q):
     run_small(W, x, label=f"D={D} K={K} Q={Q}")
 
 
-@pytest.mark.parametrize("cta_rounds,extra,K", [(1, 37, 256), (3, 11, 512), (1, 37, 384)])
-def test_pair_and_split_items_mixed(cta_rounds, extra, K):
+@pytest.mark.parametrize("cta_rounds,extra,K,metric", [(1, 37, 256, "l2"), (3, 11, 512, "l2"), (1, 37, 384, "l2"),
+                                                      (1, 37, 256, "cosine")])
+def test_pair_and_split_items_mixed(cta_rounds, extra, K, metric):
     """Tile counts just above a multiple of the SM count: some CTAs get a
     second tile in an item and the rest a lone tile, which is split between
     the CTA's two pipelines when a stage has an even number of 128-codeword
@@ -196,7 +197,7 @@ def test_pair_and_split_items_mixed(cta_rounds, extra, K):
     N = (cta_rounds * sms + extra) * 128 - 50
     w, W = _small_weights(D=64, K=K, Q=3, seed=K + extra)
     x = np.random.default_rng(K).standard_normal((N, 64)).astype(np.float32)
-    run_small(W, x, label=f"tiles={cta_rounds}x{sms}+{extra} K={K}")
+    run_small(W, x, label=f"tiles={cta_rounds}x{sms}+{extra} K={K} {metric}", metric=metric)
 
 
 def test_biases_and_prefix_depths():
@@ -274,3 +275,73 @@ def test_invalid_arguments_raise():
         rvq.encode(x, n_q=5)
     with pytest.raises(ValueError):
         rvq.encode(torch.zeros((4, 65), device=DEV))
+
+
+# ---------------------------------------------------------------------------
+# the normalised ("cosine") metric and the 8-dim code space
+# ---------------------------------------------------------------------------
+
+def test_moss_lfq_workload_every_frame():
+    """32 books of 1024 entries in an 8-dim code space, argmin between
+    L2-normalised vectors: all 12 000 frames checked on the oracle."""
+    w = ri.WORKLOAD_BY_NAME["moss_lfq"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    res, _ = run_small(W, x, label="moss_lfq", metric="cosine")
+    assert res["n_equal"] >= 0.97 * res["n_stages"]
+
+
+@pytest.mark.parametrize("D,K,Q,metric", [(16, 128, 1, "l2"), (64, 256, 3, "cosine"), (96, 384, 5, "l2"),
+                                          (256, 1024, 8, "cosine"), (48, 640, 2, "cosine"),
+                                          (128, 128, 4, "cosine"), (64, 1024, 40, "l2")])
+def test_small_code_space_shapes(D, K, Q, metric):
+    """d = 8: chunk counts 1 to 8 (split three ways across a CTA's pipelines,
+    some of which then scan nothing), both metrics, up to 40 stages."""
+    w, W = _small_weights(D=D, K=K, Q=Q, seed=D + K + Q, d=8)
+    x = np.random.default_rng(D + Q).standard_normal((300, D)).astype(np.float32)
+    run_small(W, x, label=f"d=8 D={D} K={K} Q={Q} {metric}", metric=metric)
+
+
+@pytest.mark.parametrize("metric", ["l2", "cosine"])
+def test_small_code_space_three_tile_items(metric):
+    """d = 8 with more tiles than SMs: items of three tiles, one per
+    pipeline, the last items with tiles past the end."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = (3 * sms + 5) * 128 - 77
+    w, W = _small_weights(D=64, K=256, Q=4, seed=91, d=8)
+    x = np.random.default_rng(91).standard_normal((N, 64)).astype(np.float32)
+    run_small(W, x, label=f"d=8 three-tile items {metric}", metric=metric)
+
+
+@pytest.mark.parametrize("d", [8, 64])
+def test_cosine_biases_prefix_and_scale(d):
+    """Both biases, prefix depths, and the eps floor: frames scaled down to
+    norm ~1e-14 give projections below 1e-12, where the query is divided by
+    eps instead of by its norm."""
+    w, W = _small_weights(D=128, K=512, Q=5, bias=True, seed=31, d=d)
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((400, 128)).astype(np.float32)
+    _, full = run_small(W, x, label=f"cosine d={d} bias", metric="cosine")
+    for n_q in (1, 3):
+        _, c = run_small(W, x, n_q=n_q, label=f"cosine d={d} n_q={n_q}", metric="cosine")
+        assert np.array_equal(c, full[:, :n_q]), "prefix property"
+    # the reconstruction of such frames is a sum of stored codewords, O(1)
+    # against frames of ~1e-14: its tolerance is taken on the oracle's
+    # reconstruction, as for decode-only inputs
+    W0 = dict(W, b_in=None, b_out=None)
+    tiny = (x[:200] * 1e-14).astype(np.float32)
+    rvq = make_rvq(W0, "cosine")
+    codes, x_hat = rvq.reconstruct(torch.from_numpy(tiny).to(DEV))
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    y_ref, _ = oracle.decode(W0, c)
+    check_encode(W0, tiny, c, x_rms=rms(y_ref), x_hat_gpu=x_hat.cpu().numpy(), label=f"cosine d={d} tiny frames",
+                 metric="cosine")
+
+
+def test_cosine_d64_workload_shapes():
+    """d = 64 with the normalised metric: a two-tile launch and a split one."""
+    for N, K in ((150 * 128 + 40, 1024), (300, 256)):
+        w, W = _small_weights(D=256, K=K, Q=4, seed=N % 97, d=64)
+        x = np.random.default_rng(N).standard_normal((N, 256)).astype(np.float32)
+        run_small(W, x, label=f"cosine d=64 N={N} K={K}", metric="cosine")
