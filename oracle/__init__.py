@@ -18,6 +18,10 @@ reconstruct(weights, x, n_q) -> dict(codes, ..., x_hat)
 
 `weights` is a dict of float32 numpy arrays: w_in [Q][d][D], codebook [Q][K][d],
 w_out [Q][D][d], and optionally b_in [Q][d] and b_out [Q][D] (None = zero).
+Optionally the Linear layers around the quantizer (omnivoice.cpp
+ARCHITECTURE.md, "Audio tokenizer"): fc_w [D][D_in] with fc_b [D] maps each
+frame before the residual loop (x is then [N][D_in]); fc2_w [D_out][D] with
+fc2_b [D_out] maps the decoded sum (decode then returns [N][D_out]).
 """
 
 from __future__ import annotations
@@ -60,6 +64,12 @@ def _load():
             lib.rvq_oracle_encode_metric.argtypes = ([ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int]
                                                      + [f] * 4 + [ctypes.c_int, ctypes.c_int])
             lib.rvq_oracle_encode_metric.restype = ctypes.c_int
+            lib.rvq_oracle_encode_ex.argtypes = ([ctypes.c_int] * 5 + [f] * 8 + [ctypes.c_int64, ctypes.c_int]
+                                                 + [f] * 4 + [ctypes.c_int, ctypes.c_int])
+            lib.rvq_oracle_encode_ex.restype = ctypes.c_int
+            lib.rvq_oracle_decode_ex.argtypes = ([ctypes.c_int] * 5 + [f] * 6 + [ctypes.c_int64, ctypes.c_int, f, f,
+                                                                                ctypes.c_int])
+            lib.rvq_oracle_decode_ex.restype = ctypes.c_int
             lib.rvq_oracle_decode.argtypes = [ctypes.c_int] * 4 + [f] * 4 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
             lib.rvq_oracle_decode.restype = ctypes.c_int
             lib.rvq_oracle_version.restype = ctypes.c_char_p
@@ -87,6 +97,22 @@ def _dims(weights):
     return D, d, K, Q
 
 
+def _fc_dims(weights, D):
+    """(D_in, D_out): the widths before fc and after fc2 (D where absent)."""
+    D_in, D_out = D, D
+    if weights.get("fc_w") is not None:
+        assert weights["fc_w"].shape[0] == D
+        D_in = weights["fc_w"].shape[1]
+        if weights.get("fc_b") is not None:
+            assert weights["fc_b"].shape == (D,)
+    if weights.get("fc2_w") is not None:
+        assert weights["fc2_w"].shape[1] == D
+        D_out = weights["fc2_w"].shape[0]
+        if weights.get("fc2_b") is not None:
+            assert weights["fc2_b"].shape == (D_out,)
+    return D_in, D_out
+
+
 METRICS = {"l2": 0, "cosine": 1}
 
 
@@ -95,16 +121,22 @@ def encode(weights: dict, x: np.ndarray, n_q: int | None = None, threads: int = 
     lib = _load()
     m = METRICS[metric]
     D, d, K, Q = _dims(weights)
+    D_in, _ = _fc_dims(weights, D)
     n_q = Q if n_q is None else int(n_q)
     x = _f32(x)
     N = x.shape[0]
-    assert x.shape == (N, D)
+    assert x.shape == (N, D_in)
     w = {k: _f32(weights.get(k)) for k in ("w_in", "b_in", "codebook", "w_out", "b_out")}
     codes = np.empty((N, n_q), dtype=np.int32)
     gap = np.empty((N, n_q), dtype=np.float64)
     best = np.empty((N, n_q), dtype=np.float64)
     resid = np.empty((N, D), dtype=np.float64) if want_residual else None
-    if m == 0:
+    if weights.get("fc_w") is not None:
+        fc_w, fc_b = _f32(weights["fc_w"]), _f32(weights.get("fc_b"))
+        rc = lib.rvq_oracle_encode_ex(D_in, D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
+                                      _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(fc_w), _ptr(fc_b), _ptr(x), N, n_q,
+                                      _ptr(codes), _ptr(gap), _ptr(best), _ptr(resid), m, int(threads))
+    elif m == 0:
         rc = lib.rvq_oracle_encode(D, d, K, Q, _ptr(w["w_in"]), _ptr(w["b_in"]), _ptr(w["codebook"]),
                                    _ptr(w["w_out"]), _ptr(w["b_out"]), _ptr(x), N, n_q, _ptr(codes),
                                    _ptr(gap), _ptr(best), _ptr(resid), int(threads))
@@ -124,11 +156,17 @@ def decode(weights: dict, codes: np.ndarray, n_q: int | None = None, threads: in
     N = codes.shape[0]
     n_q = codes.shape[1] if n_q is None else int(n_q)
     assert codes.shape == (N, n_q)
-    w = {k: _f32(weights.get(k)) for k in ("codebook", "w_out", "b_out")}
-    y = np.empty((N, D), dtype=np.float64)
+    w = {k: _f32(weights.get(k)) for k in ("codebook", "w_out", "b_out", "fc2_w", "fc2_b")}
+    _, D_out = _fc_dims(weights, D)
+    y = np.empty((N, D_out), dtype=np.float64)
     n_bad = ctypes.c_int64(0)
-    rc = lib.rvq_oracle_decode(D, d, K, Q, _ptr(w["codebook"]), _ptr(w["w_out"]), _ptr(w["b_out"]),
-                               _ptr(codes), N, n_q, _ptr(y), ctypes.addressof(n_bad), int(threads))
+    if w["fc2_w"] is not None:
+        rc = lib.rvq_oracle_decode_ex(D, D_out, d, K, Q, _ptr(w["codebook"]), _ptr(w["w_out"]), _ptr(w["b_out"]),
+                                      _ptr(w["fc2_w"]), _ptr(w["fc2_b"]), _ptr(codes), N, n_q, _ptr(y),
+                                      ctypes.addressof(n_bad), int(threads))
+    else:
+        rc = lib.rvq_oracle_decode(D, d, K, Q, _ptr(w["codebook"]), _ptr(w["w_out"]), _ptr(w["b_out"]),
+                                   _ptr(codes), N, n_q, _ptr(y), ctypes.addressof(n_bad), int(threads))
     if rc != 0:
         raise ValueError("rvq_oracle_decode rejected its arguments")
     return y, int(n_bad.value)

@@ -30,6 +30,11 @@
 //     can tell near-ties from clear decisions;
 //   * decode codes outside [0, K) contribute nothing and are counted.
 //
+// Optional Linear layers around the quantizer (omnivoice.cpp ARCHITECTURE.md,
+// "Audio tokenizer" data flow and tensor table): fc (D_in -> D) maps the frame
+// to the quantizer's input before the residual loop, fc2 (D -> D_out) maps the
+// decoded sum afterwards; both are weight [out][in] plus bias, in float64.
+//
 // The normalised metric (metric 1) is the quantizer of moss-tts.cpp AGENTS.md,
 // gotcha 9: both the projected encoding and every codeword are L2-normalised,
 // v / max(||v||_2, 1e-12), before the argmin; decode stays gather + sum, so
@@ -141,25 +146,39 @@ void encode_frame(const Weights &W, int n_q, int metric, std::vector<double> &re
 
 extern "C" {
 
-// Encode N frames with the first n_q stages.
+// Encode N frames [N][D_in] with the first n_q stages; with fc_w, the frame is
+// first mapped by fc (fc_w [D][D_in], fc_b [D] nullable), otherwise D_in == D.
 //   metric    0: squared L2; 1: squared L2 between L2-normalised vectors
 //   codes     [N][n_q] int32   (required)
 //   gap       [N][n_q] float64 relative gap (d2-d1)/d2 per stage (nullable)
 //   best_dist [N][n_q] float64 best squared distance per stage (nullable)
 //   residual  [N][D]   float64 final residual (nullable)
 // Returns 0 on success, -1 on a bad argument.
-int rvq_oracle_encode_metric(int D, int d, int K, int Q, const float *w_in, const float *b_in,
-                             const float *codebook, const float *w_out, const float *b_out,
-                             const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
-                             double *best_dist, double *residual, int metric, int threads) {
+int rvq_oracle_encode_ex(int D_in, int D, int d, int K, int Q, const float *w_in, const float *b_in,
+                         const float *codebook, const float *w_out, const float *b_out, const float *fc_w,
+                         const float *fc_b, const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
+                         double *best_dist, double *residual, int metric, int threads) {
   if (D <= 0 || d <= 0 || K <= 0 || Q <= 0 || N < 0 || n_q < 1 || n_q > Q) return -1;
   if (metric != 0 && metric != 1) return -1;
+  if (D_in <= 0 || (!fc_w && D_in != D)) return -1;
   if (!w_in || !codebook || !w_out || (!x && N > 0) || (!codes && N > 0)) return -1;
   Weights W{D, d, K, Q, w_in, b_in, codebook, w_out, b_out};
   parallel_frames(N, threads, [&](int64_t lo, int64_t hi) {
     std::vector<double> r((size_t)D), e((size_t)d), c_n((size_t)d);
     for (int64_t n = lo; n < hi; ++n) {
-      for (int i = 0; i < D; ++i) r[i] = (double)x[(size_t)n * D + i];
+      const float *xn = x + (size_t)n * D_in;
+      if (fc_w) {
+        // residual = fc(x) = fc_w . x + fc_b
+        for (int i = 0; i < D; ++i) {
+          double s = 0.0;
+          const float *row = fc_w + (size_t)i * D_in;
+          for (int j = 0; j < D_in; ++j) s += (double)row[j] * (double)xn[j];
+          if (fc_b) s += (double)fc_b[i];
+          r[i] = s;
+        }
+      } else {
+        for (int i = 0; i < D; ++i) r[i] = (double)xn[i];
+      }
       encode_frame(W, n_q, metric, r, e, c_n, codes + (size_t)n * n_q, gap ? gap + (size_t)n * n_q : nullptr,
                    best_dist ? best_dist + (size_t)n * n_q : nullptr);
       if (residual)
@@ -169,7 +188,16 @@ int rvq_oracle_encode_metric(int D, int d, int K, int Q, const float *w_in, cons
   return 0;
 }
 
-// Squared-L2 encode (metric 0).
+// Without fc.
+int rvq_oracle_encode_metric(int D, int d, int K, int Q, const float *w_in, const float *b_in,
+                             const float *codebook, const float *w_out, const float *b_out,
+                             const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
+                             double *best_dist, double *residual, int metric, int threads) {
+  return rvq_oracle_encode_ex(D, D, d, K, Q, w_in, b_in, codebook, w_out, b_out, nullptr, nullptr, x, N, n_q,
+                              codes, gap, best_dist, residual, metric, threads);
+}
+
+// Squared-L2 encode (metric 0), without fc.
 int rvq_oracle_encode(int D, int d, int K, int Q, const float *w_in, const float *b_in,
                       const float *codebook, const float *w_out, const float *b_out,
                       const float *x, int64_t N, int n_q, int32_t *codes, double *gap,
@@ -178,18 +206,21 @@ int rvq_oracle_encode(int D, int d, int K, int Q, const float *w_in, const float
                                   best_dist, residual, 0, threads);
 }
 
-// Decode N frames of codes [N][n_q] into y [N][D] float64:
-//   y[n] = sum_{k < n_q} ( w_out[k] . codebook[k][codes[n][k]] + b_out[k] ).
+// Decode N frames of codes [N][n_q] into y [N][D_out] float64:
+//   s[n] = sum_{k < n_q} ( w_out[k] . codebook[k][codes[n][k]] + b_out[k] ),
+//   y[n] = fc2_w . s[n] + fc2_b  (fc2_w [D_out][D], fc2_b nullable)  or  s[n] (D_out == D).
 // A code outside [0, K) contributes nothing and is counted in *n_bad.
-int rvq_oracle_decode(int D, int d, int K, int Q, const float *codebook, const float *w_out,
-                      const float *b_out, const int32_t *codes, int64_t N, int n_q, double *y,
-                      int64_t *n_bad, int threads) {
+int rvq_oracle_decode_ex(int D, int D_out, int d, int K, int Q, const float *codebook, const float *w_out,
+                         const float *b_out, const float *fc2_w, const float *fc2_b, const int32_t *codes,
+                         int64_t N, int n_q, double *y, int64_t *n_bad, int threads) {
   if (D <= 0 || d <= 0 || K <= 0 || Q <= 0 || N < 0 || n_q < 1 || n_q > Q) return -1;
+  if (D_out <= 0 || (!fc2_w && D_out != D)) return -1;
   if (!codebook || !w_out || (!codes && N > 0) || (!y && N > 0)) return -1;
   std::vector<int64_t> bad_per_frame((size_t)std::max<int64_t>(N, 1), 0);
   parallel_frames(N, threads, [&](int64_t lo, int64_t hi) {
+    std::vector<double> sum((size_t)D);
     for (int64_t n = lo; n < hi; ++n) {
-      double *acc = y + (size_t)n * D;
+      double *acc = fc2_w ? sum.data() : y + (size_t)n * D;
       for (int i = 0; i < D; ++i) acc[i] = 0.0;
       for (int k = 0; k < n_q; ++k) {
         int32_t code = codes[(size_t)n * n_q + k];
@@ -207,6 +238,17 @@ int rvq_oracle_decode(int D, int d, int K, int Q, const float *codebook, const f
           acc[i] += s;
         }
       }
+      if (fc2_w) {
+        // y = fc2(s) = fc2_w . s + fc2_b
+        double *out = y + (size_t)n * D_out;
+        for (int i = 0; i < D_out; ++i) {
+          double t = 0.0;
+          const float *row = fc2_w + (size_t)i * D;
+          for (int j = 0; j < D; ++j) t += (double)row[j] * acc[j];
+          if (fc2_b) t += (double)fc2_b[i];
+          out[i] = t;
+        }
+      }
     }
   });
   if (n_bad) {
@@ -217,6 +259,14 @@ int rvq_oracle_decode(int D, int d, int K, int Q, const float *codebook, const f
   return 0;
 }
 
-const char *rvq_oracle_version(void) { return "rvq-oracle f64 2"; }
+// Without fc2.
+int rvq_oracle_decode(int D, int d, int K, int Q, const float *codebook, const float *w_out,
+                      const float *b_out, const int32_t *codes, int64_t N, int n_q, double *y,
+                      int64_t *n_bad, int threads) {
+  return rvq_oracle_decode_ex(D, D, d, K, Q, codebook, w_out, b_out, nullptr, nullptr, codes, N, n_q, y, n_bad,
+                              threads);
+}
+
+const char *rvq_oracle_version(void) { return "rvq-oracle f64 3"; }
 
 }  // extern "C"

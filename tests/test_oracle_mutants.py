@@ -36,6 +36,13 @@ MUTANTS = {
         "double nn = 0; for (int j = 0; j < d; ++j) nn += (double)c[j] * c[j];\n"
         "      for (int j = 0; j < d; ++j) s += (double)row[j] * (double)c[j] / (metric == 1 ? std::sqrt(nn) : 1.0);\n"
         "      if (W.b_out)"),
+    # the Linear layers around the quantizer
+    "fc_bias_dropped": ("if (fc_b) s += (double)fc_b[i];", "if (false) s += (double)fc_b[i];"),
+    "fc_transposed": ("for (int j = 0; j < D_in; ++j) s += (double)row[j] * (double)xn[j];",
+                      "for (int j = 0; j < D_in; ++j) s += (double)fc_w[(size_t)j * D + i] * (double)xn[j];"),
+    "fc2_bias_dropped": ("if (fc2_b) t += (double)fc2_b[i];", "if (false) t += (double)fc2_b[i];"),
+    "fc2_transposed": ("for (int j = 0; j < D; ++j) t += (double)row[j] * acc[j];",
+                       "for (int j = 0; j < D; ++j) t += (double)fc2_w[(size_t)j * D_out + i] * acc[j];"),
 }
 
 PINS = [
@@ -56,6 +63,8 @@ PINS = [
     pins.test_cosine_single_stage_is_scipy_cosine_neighbour,
     pins.test_cosine_scale_invariance_of_one_stage,
     pins.test_cosine_planted_recovery_exact,
+    pins.test_fc_maps_frames_before_the_loop,
+    pins.test_fc2_maps_the_decoded_sum,
 ]
 
 
@@ -78,6 +87,11 @@ def _configure(lib):
     lib.rvq_oracle_encode_metric.argtypes = ([ctypes.c_int] * 4 + [f] * 6 + [ctypes.c_int64, ctypes.c_int] + [f] * 4
                                              + [ctypes.c_int, ctypes.c_int])
     lib.rvq_oracle_encode_metric.restype = ctypes.c_int
+    lib.rvq_oracle_encode_ex.argtypes = ([ctypes.c_int] * 5 + [f] * 8 + [ctypes.c_int64, ctypes.c_int] + [f] * 4
+                                         + [ctypes.c_int, ctypes.c_int])
+    lib.rvq_oracle_encode_ex.restype = ctypes.c_int
+    lib.rvq_oracle_decode_ex.argtypes = [ctypes.c_int] * 5 + [f] * 6 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
+    lib.rvq_oracle_decode_ex.restype = ctypes.c_int
     lib.rvq_oracle_decode.argtypes = [ctypes.c_int] * 4 + [f] * 4 + [ctypes.c_int64, ctypes.c_int, f, f, ctypes.c_int]
     lib.rvq_oracle_decode.restype = ctypes.c_int
     lib.rvq_oracle_version.restype = ctypes.c_char_p
@@ -99,7 +113,7 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
 
 
 def test_unmutated_copy_passes_every_pin(tmp_path, monkeypatch):
-    lib = _configure(ctypes.CDLL(_build_mutant(tmp_path, "identity", "rvq-oracle f64 2", "rvq-oracle f64 2")))
+    lib = _configure(ctypes.CDLL(_build_mutant(tmp_path, "identity", "rvq-oracle f64 3", "rvq-oracle f64 3")))
     monkeypatch.setattr(oracle, "_lib", lib)
     for pin in PINS:
         pin()

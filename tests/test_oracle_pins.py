@@ -427,3 +427,57 @@ def test_cosine_planted_recovery_exact():
     assert np.abs(res["residual"]).max() < 1e-5   # float32 weights: exact up to their rounding
     y, _ = oracle.decode(W, res["codes"])
     assert np.abs(y - x).max() < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# the Linear layers around the quantizer (omnivoice.cpp ARCHITECTURE.md,
+# "Audio tokenizer"): fc before the residual loop, fc2 after the decoded sum.
+# Integer weights and frames keep every product exact in float32 and float64.
+# ---------------------------------------------------------------------------
+
+def _int_rvq(rng, Q, d, D, K):
+    w_in = rng.integers(-2, 3, size=(Q, d, D)).astype(np.float64)
+    w_out = rng.integers(-2, 3, size=(Q, D, d)).astype(np.float64)
+    cb = rng.integers(-4, 5, size=(Q, K, d)).astype(np.float64)
+    return w_in, cb, w_out
+
+
+def test_fc_maps_frames_before_the_loop():
+    """With fc (a non-square, non-symmetric integer D x D_in matrix plus an
+    integer bias) the codes, distances and final residual equal those of the
+    plain loop run on fc(x) = fc_w x + fc_b, computed exactly here."""
+    rng = np.random.default_rng(21)
+    Q, d, D, D_in, K, N = 3, 3, 5, 7, 9, 200
+    w_in, cb, w_out = _int_rvq(rng, Q, d, D, K)
+    fc_w = rng.integers(-3, 4, size=(D, D_in)).astype(np.float64)
+    fc_b = rng.integers(-5, 6, size=(D,)).astype(np.float64)
+    x = rng.integers(-4, 5, size=(N, D_in)).astype(np.float64)
+    xp = (x.astype(np.int64) @ fc_w.astype(np.int64).T + fc_b.astype(np.int64)).astype(np.float64)
+    W = _weights(w_in, cb, w_out)
+    Wfc = dict(W, fc_w=np.float32(fc_w), fc_b=np.float32(fc_b))
+    a = oracle.encode(Wfc, x)
+    b = oracle.encode(W, xp)
+    assert np.array_equal(a["codes"], b["codes"])
+    assert np.array_equal(a["best_dist"], b["best_dist"])
+    assert np.array_equal(a["residual"], b["residual"])
+    # and fc changes the result (the test is not vacuous)
+    assert not np.array_equal(oracle.encode(W, x[:, :D])["codes"], a["codes"])
+
+
+def test_fc2_maps_the_decoded_sum():
+    """decode with fc2 = fc2_w (sum of the stage outputs) + fc2_b, the bias
+    once (three stages), against fc2 applied exactly to the plain decode."""
+    rng = np.random.default_rng(22)
+    Q, d, D, D_out, K, N = 3, 2, 6, 4, 7, 150
+    w_in, cb, w_out = _int_rvq(rng, Q, d, D, K)
+    b_out = rng.integers(-3, 4, size=(Q, D)).astype(np.float64)
+    fc2_w = rng.integers(-3, 4, size=(D_out, D)).astype(np.float64)
+    fc2_b = rng.integers(-5, 6, size=(D_out,)).astype(np.float64)
+    codes = rng.integers(0, K, size=(N, Q)).astype(np.int32)
+    W = _weights(w_in, cb, w_out, b_out=b_out)
+    y, bad = oracle.decode(W, codes)
+    y2, bad2 = oracle.decode(dict(W, fc2_w=np.float32(fc2_w), fc2_b=np.float32(fc2_b)), codes)
+    want = (y.astype(np.int64) @ fc2_w.astype(np.int64).T + fc2_b.astype(np.int64)).astype(np.float64)
+    assert bad == bad2 == 0
+    assert y2.shape == (N, D_out)
+    assert np.array_equal(y2, want)
