@@ -56,13 +56,13 @@ def _peaks():
 
 
 def encode_flops_per_frame(w) -> float:
-    # stage projections (2*D*d per stage) + distances (2*K*d per stage)
-    return w.Q * (2.0 * w.D * w.d + 2.0 * w.K * w.d)
+    # stage projections (2*D_in*d per stage, fc folded in) + distances (2*K*d per stage)
+    return w.Q * (2.0 * w.D_in * w.d + 2.0 * w.K * w.d)
 
 
 def decode_bytes_per_frame(w) -> float:
-    # read n_q int32 codes, write D float32 outputs
-    return 4.0 * (w.Q + w.D)
+    # read n_q int32 codes, write D_out float32 outputs
+    return 4.0 * (w.Q + w.D_out)
 
 
 class ClockSampler:
@@ -190,13 +190,14 @@ def run_ours(args):
         w = dataclasses.replace(w, B=1, T=args.frames)
     W = ri.make_weights(w)
     Wt = ri.weights_to_torch(W, dev)
-    rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev, metric=w.metric)
+    rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev, metric=w.metric,
+                 fc_w=Wt.get("fc_w"), fc_b=Wt.get("fc_b"), fc2_w=Wt.get("fc2_w"), fc2_b=Wt.get("fc2_b"))
     # each rank encodes its own batch of the workload's shape: shift the frame seed per rank
     wr = dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
     x = ri.make_x_torch(wr, Wt, dev)
     N, n_q = w.N, w.Q
     codes = torch.empty((N, n_q), dtype=torch.int32, device=dev)
-    y = torch.empty((N, w.D), dtype=torch.float32, device=dev)
+    y = torch.empty((N, w.D_out), dtype=torch.float32, device=dev)
     scratch = rvq.scratch_for(N, n_q)
     stream = torch.cuda.current_stream(dev)
 
@@ -300,8 +301,9 @@ def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, cloc
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.describe(), "frames_per_gpu": N, "parallelism": f"replicas{world}",
-                   "l2": (f"input and output {N * w.D * 4 / 1e6:.0f} MB each, "
-                         + ("larger than L2; no flush" if N * w.D * 4 > L2_BYTES else "L2-resident (profiling case)")),
+                   "l2": (f"input {N * w.D_in * 4 / 1e6:.0f} MB, output {N * w.D_out * 4 / 1e6:.0f} MB, "
+                         + ("larger than L2; no flush" if N * min(w.D_in, w.D_out) * 4 > L2_BYTES
+                            else "L2-resident (profiling case)")),
                    "step": "rvq_encode + rvq_decode through the C ABI"},
         "encode_ms": enc_ms, "decode_ms": dec_ms,
         "encode_frames_per_s": N / (enc_ms / 1e3), "decode_frames_per_s": N / (dec_ms / 1e3),
@@ -318,7 +320,7 @@ def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, cloc
         "cpu_baseline": cpu,
         "e2e": None if e2e_ms is None else {
             "value": world * N / (e2e_ms / 1e3), "unit": "frames/s",
-            "h2d_bytes_per_step": N * w.D * 4, "d2h_bytes_per_step": N * w.D * 4 + N * n_q * 4,
+            "h2d_bytes_per_step": N * w.D_in * 4, "d2h_bytes_per_step": N * w.D_out * 4 + N * n_q * 4,
             "api": "rvq_pipeline_reconstruct (pinned host buffers, copies overlapped with compute)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
@@ -401,9 +403,11 @@ def per_workload_table(args):
     for w in ri.WORKLOADS:
         W = ri.make_weights(w)
         Wt = ri.weights_to_torch(W, dev)
-        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], device=dev, metric=w.metric)
+        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], device=dev, metric=w.metric, fc_w=Wt.get("fc_w"),
+                     fc_b=Wt.get("fc_b"), fc2_w=Wt.get("fc2_w"), fc2_b=Wt.get("fc2_b"))
         n_q = w.Q
-        row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q, "K": w.K, "d": w.d, "metric": w.metric}
+        row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q, "K": w.K, "d": w.d, "metric": w.metric,
+               "D_in": w.D_in, "D_out": w.D_out}
         if w.kind == "decode":
             codes = torch.from_numpy(ri.make_codes(w)).to(dev)
             x_host = None
@@ -411,7 +415,7 @@ def per_workload_table(args):
             x = ri.make_x_torch(w, Wt, dev) if w.N > 20000 else torch.from_numpy(ri.make_x(w, W)).to(dev)
             codes = torch.empty((w.N, n_q), dtype=torch.int32, device=dev)
             scratch = rvq.scratch_for(w.N, n_q)
-        y = torch.empty((w.N, w.D), dtype=torch.float32, device=dev)
+        y = torch.empty((w.N, w.D_out), dtype=torch.float32, device=dev)
 
         def timed(fn, reps=10):
             for _ in range(3):

@@ -22,13 +22,20 @@
  * n(v) = max(||v||_2, 1e-12) (moss-tts.cpp AGENTS.md, gotcha 9: the quantizer
  * L2-normalises the projected encoding and the codebook before the argmin in
  * code space); the residual update and decode still use the stored codeword.
+ * Optionally the Linear layers around the quantizer in that codec
+ * (omnivoice.cpp ARCHITECTURE.md, "Audio tokenizer" data flow: fc 1024 -> 1024
+ * before the RVQ encode, fc2 1024 -> 256 after the RVQ decode) are folded
+ * into the tables: encode then takes frames of width D_in and maps each by
+ * fc (x' = fc_w . x + fc_b) before the loop, and decode returns
+ * fc2_w . y + fc2_b, of width D_out.
  *
  * Shapes and layouts (all float32 row-major, PyTorch (out, in) layouts as in
  * that section's tensor table):
  *   w_in     [Q][d][D]      b_in  [Q][d]  (nullable: zero)
  *   codebook [Q][K][d]
  *   w_out    [Q][D][d]      b_out [Q][D]  (nullable: zero)
- *   x, y, x_hat [N][D]      frame-major: one contiguous feature vector per frame
+ *   fc_w [D][D_in], fc_b [D]; fc2_w [D_out][D], fc2_b [D_out]   (all nullable)
+ *   x [N][D_in], y and x_hat [N][D_out]   frame-major: one contiguous vector per frame
  *   codes    [N][n_q] int32 frame-major (moss-tts.cpp AGENTS.md, gotcha 8)
  *
  * Memory and ownership.  Every pointer except the struct pointers is DEVICE
@@ -87,25 +94,37 @@ typedef enum rvq_status {
   RVQ_ERR_TIMEOUT = -5
 } rvq_status;
 
-/* D: frame (feature) dimension; d: code-space dimension; K: entries per
- * codebook; Q: number of stages held in the tables; metric: RVQ_METRIC_L2 or
- * RVQ_METRIC_COSINE (an initialiser that leaves it out gives RVQ_METRIC_L2).
- * Tables prepared for one metric serve only that metric. */
+/* D: the quantizer's input (residual) dimension; d: code-space dimension;
+ * K: entries per codebook; Q: number of stages held in the tables; metric:
+ * RVQ_METRIC_L2 or RVQ_METRIC_COSINE; D_in: width of the frames given to
+ * encode (with fc; 0 or D without); D_out: width of decode's output (with
+ * fc2; 0 or D without).  An initialiser that leaves out the last three gives
+ * RVQ_METRIC_L2 and no fc or fc2.  Tables prepared for one set of dims serve
+ * only those dims. */
 typedef struct rvq_dims {
   int32_t D;
   int32_t d;
   int32_t K;
   int32_t Q;
   int32_t metric;
+  int32_t D_in;
+  int32_t D_out;
 } rvq_dims;
 
-/* Device pointers to the per-stage tensors (layouts above). */
+/* Device pointers to the per-stage tensors and the optional Linear layers
+ * (layouts above).  fc_w must be given when dims.D_in is neither 0 nor D,
+ * and fc2_w when dims.D_out is neither 0 nor D; when given they are used
+ * (even at D_in == D or D_out == D). */
 typedef struct rvq_weights {
   const float *w_in;
   const float *b_in;
   const float *codebook;
   const float *w_out;
   const float *b_out;
+  const float *fc_w;
+  const float *fc_b;
+  const float *fc2_w;
+  const float *fc2_b;
 } rvq_weights;
 
 /* Same type as cudaStream_t; the header needs no CUDA include.  NULL is the
@@ -117,7 +136,8 @@ typedef struct CUstream_st *rvq_stream_t;
  * RVQ_ERR_INVALID_ARG for non-positive values or an unknown metric).
  * Supported: d == 64 with K a multiple of 128, K <= 65536; or d == 8 with K
  * a multiple of 128, K <= 1024 (two stages' codebooks stay on chip);
- * D a multiple of 16 with D <= 16384; 1 <= Q <= 64; either metric. */
+ * D, and D_in and D_out when non-zero, multiples of 16 up to 16384;
+ * 1 <= Q <= 64; either metric. */
 RVQ_API rvq_status rvq_dims_supported(rvq_dims dims);
 
 /* Bytes of the tables buffer for these dims (0 if unsupported). */
@@ -133,7 +153,10 @@ RVQ_API size_t rvq_tables_bytes(rvq_dims dims);
  * which lets encode update every stage's projection without materialising the
  * D-dimensional residual:  w_in[q] . residual_q = w_in[q] . x - sum_{s<q} G[q][s][code_s].
  * Both are exact re-associations of the sums in the "RVQ codec" section.
- * Also a copy of w_in split into TF32 high and low parts, and -2 x the
+ * With fc, the projections read fc_w-mapped frames: w_in[q] . fc_w (and
+ * w_in[q] . fc_b + b_in[q]) replace w_in[q] (and b_in[q]); with fc2, Z holds
+ * fc2_w . Z[q][k] ([Q][K][D_out]) and fc2_b is added once per frame.
+ * Also a copy of w_in (with fc folded in) split into TF32 high and low parts, and -2 x the
  * codebook (normalised first for RVQ_METRIC_COSINE) split the same way, in the
  * layouts the kernels read.  Asynchronous on `stream`. */
 RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *tables,
@@ -153,7 +176,7 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
 RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q);
 RVQ_API size_t rvq_encode_min_scratch_bytes(rvq_dims dims, int32_t n_q);
 
-/* Encode n_frames frames x [N][D] with the first n_q stages (1 <= n_q <= Q)
+/* Encode n_frames frames x [N][D_in] with the first n_q stages (1 <= n_q <= Q)
  * into codes [N][n_q].  Each code is the argmin of the squared L2 distance,
  * lowest index on ties.  The distances are computed to about float32
  * accuracy; where two entries' distances differ by less than that, either
@@ -162,8 +185,9 @@ RVQ_API rvq_status rvq_encode(rvq_dims dims, const void *tables, const float *x,
                               int32_t n_q, int32_t *codes, void *scratch, size_t scratch_bytes,
                               rvq_stream_t stream);
 
-/* Decode codes [N][n_q] into y [N][D]:
- *   y[n] = sum_{q < n_q} Z[q][codes[n][q]]   (summed in stage order, float32).
+/* Decode codes [N][n_q] into y [N][D_out]:
+ *   y[n] = fc2_b + sum_{q < n_q} Z[q][codes[n][q]]   (summed in stage order,
+ *   float32; fc2_b is zero without fc2).
  * A code outside [0, K) contributes nothing; if bad_codes (device, int64) is
  * not NULL, the number of such codes is added to *bad_codes (atomically; the
  * caller zeroes it). */
@@ -171,8 +195,9 @@ RVQ_API rvq_status rvq_decode(rvq_dims dims, const void *tables, const int32_t *
                               int64_t n_frames, int32_t n_q, float *y, int64_t *bad_codes,
                               rvq_stream_t stream);
 
-/* Encode then decode: codes [N][n_q] (required) and x_hat [N][D] = decode(codes),
- * the quantised reconstruction of x (x - x_hat is the final residual). */
+/* Encode then decode: codes [N][n_q] (required) and x_hat [N][D_out] =
+ * decode(codes), the quantised reconstruction of x (without fc and fc2,
+ * x - x_hat is the final residual). */
 RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const float *x,
                                    int64_t n_frames, int32_t n_q, int32_t *codes, float *x_hat,
                                    void *scratch, size_t scratch_bytes, rvq_stream_t stream);
@@ -201,8 +226,8 @@ RVQ_API rvq_status rvq_pipeline_create(rvq_dims dims, int32_t n_q, int64_t chunk
 /* Wait for the pipeline's work, release its streams and events, free it. */
 RVQ_API rvq_status rvq_pipeline_destroy(rvq_pipeline *pipeline);
 
-/* Encode and decode n_frames host frames x_host [N][D] with the tables of
- * rvq_prepare: codes_host [N][n_q] (required) and x_hat_host [N][D]
+/* Encode and decode n_frames host frames x_host [N][D_in] with the tables of
+ * rvq_prepare: codes_host [N][n_q] (required) and x_hat_host [N][D_out]
  * (nullable).  Synchronous: returns when every output is in host memory. */
 RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *pipeline, const void *tables, const float *x_host,
                                             int64_t n_frames, int32_t *codes_host, float *x_hat_host);

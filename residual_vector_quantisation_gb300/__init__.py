@@ -60,12 +60,13 @@ METRICS = {"l2": RVQ_METRIC_L2, "cosine": RVQ_METRIC_COSINE}
 
 class rvq_dims(ctypes.Structure):
     _fields_ = [("D", ctypes.c_int32), ("d", ctypes.c_int32), ("K", ctypes.c_int32), ("Q", ctypes.c_int32),
-                ("metric", ctypes.c_int32)]
+                ("metric", ctypes.c_int32), ("D_in", ctypes.c_int32), ("D_out", ctypes.c_int32)]
 
 
 class rvq_weights(ctypes.Structure):
     _fields_ = [("w_in", ctypes.c_void_p), ("b_in", ctypes.c_void_p), ("codebook", ctypes.c_void_p),
-                ("w_out", ctypes.c_void_p), ("b_out", ctypes.c_void_p)]
+                ("w_out", ctypes.c_void_p), ("b_out", ctypes.c_void_p), ("fc_w", ctypes.c_void_p),
+                ("fc_b", ctypes.c_void_p), ("fc2_w", ctypes.c_void_p), ("fc2_b", ctypes.c_void_p)]
 
 
 _lib = None
@@ -137,8 +138,8 @@ def _check(name: str, status: int):
         raise RVQError(name, status)
 
 
-def _dims(D: int, d: int, K: int, Q: int, metric: int = RVQ_METRIC_L2) -> rvq_dims:
-    return rvq_dims(int(D), int(d), int(K), int(Q), int(metric))
+def _dims(D: int, d: int, K: int, Q: int, metric: int = RVQ_METRIC_L2, D_in: int = 0, D_out: int = 0) -> rvq_dims:
+    return rvq_dims(int(D), int(d), int(K), int(Q), int(metric), int(D_in), int(D_out))
 
 
 def rvq_dims_supported(dims: rvq_dims) -> int:
@@ -157,8 +158,10 @@ def rvq_encode_min_scratch_bytes(dims: rvq_dims, n_q: int) -> int:
     return load_library().rvq_encode_min_scratch_bytes(dims, int(n_q))
 
 
-def rvq_prepare(dims: rvq_dims, w_in, codebook, w_out, b_in, b_out, tables: torch.Tensor, stream=None) -> None:
-    w = rvq_weights(_ptr(w_in), _ptr(b_in), _ptr(codebook), _ptr(w_out), _ptr(b_out))
+def rvq_prepare(dims: rvq_dims, w_in, codebook, w_out, b_in, b_out, tables: torch.Tensor, stream=None,
+                fc_w=None, fc_b=None, fc2_w=None, fc2_b=None) -> None:
+    w = rvq_weights(_ptr(w_in), _ptr(b_in), _ptr(codebook), _ptr(w_out), _ptr(b_out), _ptr(fc_w), _ptr(fc_b),
+                    _ptr(fc2_w), _ptr(fc2_b))
     _check("rvq_prepare", load_library().rvq_prepare(dims, ctypes.byref(w), _ptr(tables),
                                                      tables.numel() * tables.element_size(), _stream(stream)))
 
@@ -239,25 +242,31 @@ class RVQ:
     b_out [Q][D] or None; float32 tensors (moved to `device` if needed).
     metric: "l2" (squared L2) or "cosine" (both sides L2-normalised before the
     argmin, as RVQ_METRIC_COSINE in include/rvq.h).
+    fc_w [D][D_in], fc_b [D] (optional): a Linear layer applied to each frame
+    before the quantizer; fc2_w [D_out][D], fc2_b [D_out] (optional): one
+    applied to the decoded sum.  Both are folded into the tables.
     """
 
     def __init__(self, w_in, codebook, w_out, b_in=None, b_out=None, device=None, stream=None,
-                 metric: str = "l2"):
+                 metric: str = "l2", fc_w=None, fc_b=None, fc2_w=None, fc2_b=None):
         device = torch.device(device) if device is not None else (w_in.device if w_in.is_cuda else torch.device("cuda"))
         f = lambda t: None if t is None else t.to(device=device, dtype=torch.float32).contiguous()
         w_in, codebook, w_out, b_in, b_out = map(f, (w_in, codebook, w_out, b_in, b_out))
+        fc_w, fc_b, fc2_w, fc2_b = map(f, (fc_w, fc_b, fc2_w, fc2_b))
         Q, d, D = w_in.shape
         K = codebook.shape[1]
         self.D, self.d, self.K, self.Q = D, d, K, Q
+        self.D_in = fc_w.shape[1] if fc_w is not None else D
+        self.D_out = fc2_w.shape[0] if fc2_w is not None else D
         self.device = device
         self.metric = metric
-        self.dims = _dims(D, d, K, Q, METRICS[metric])
+        self.dims = _dims(D, d, K, Q, METRICS[metric], self.D_in, self.D_out)
         status = rvq_dims_supported(self.dims)
         _check("rvq_dims_supported", status)
         nbytes = rvq_tables_bytes(self.dims)
         self.tables = torch.empty(nbytes, dtype=torch.uint8, device=device)
         with torch.cuda.device(device):
-            rvq_prepare(self.dims, w_in, codebook, w_out, b_in, b_out, self.tables, stream)
+            rvq_prepare(self.dims, w_in, codebook, w_out, b_in, b_out, self.tables, stream, fc_w, fc_b, fc2_w, fc2_b)
         self._scratch = None
 
     def scratch_for(self, n_frames: int, n_q: int) -> torch.Tensor:
@@ -267,8 +276,8 @@ class RVQ:
         return self._scratch
 
     def _frames(self, x):
-        if x.dim() != 2 or x.shape[1] != self.D:
-            raise ValueError(f"x must be [N][{self.D}]")
+        if x.dim() != 2 or x.shape[1] != self.D_in:
+            raise ValueError(f"x must be [N][{self.D_in}]")
         return x.to(device=self.device, dtype=torch.float32).contiguous()
 
     def encode(self, x, n_q: Optional[int] = None, codes=None, stream=None):
@@ -283,7 +292,7 @@ class RVQ:
         codes = codes.to(device=self.device, dtype=torch.int32).contiguous()
         n_q = codes.shape[1] if n_q is None else int(n_q)
         if y is None:
-            y = torch.empty((codes.shape[0], self.D), dtype=torch.float32, device=self.device)
+            y = torch.empty((codes.shape[0], self.D_out), dtype=torch.float32, device=self.device)
         rvq_decode(self.dims, self.tables, codes, n_q, y, bad_codes, stream)
         return y
 
@@ -294,7 +303,7 @@ class RVQ:
         if codes is None:
             codes = torch.empty((n, n_q), dtype=torch.int32, device=self.device)
         if x_hat is None:
-            x_hat = torch.empty((n, self.D), dtype=torch.float32, device=self.device)
+            x_hat = torch.empty((n, self.D_out), dtype=torch.float32, device=self.device)
         rvq_reconstruct(self.dims, self.tables, x, n_q, codes, x_hat, self.scratch_for(n, n_q), stream)
         return codes, x_hat
 
@@ -322,7 +331,7 @@ class RVQPipeline:
         if codes_host is None:
             codes_host = torch.empty((n, self.n_q), dtype=torch.int32, pin_memory=True)
         if x_hat_host is None and want_x_hat:
-            x_hat_host = torch.empty((n, self.rvq.D), dtype=torch.float32, pin_memory=True)
+            x_hat_host = torch.empty((n, self.rvq.D_out), dtype=torch.float32, pin_memory=True)
         with torch.cuda.device(self.rvq.device):
             rvq_pipeline_reconstruct(self.handle, self.rvq.tables, x_host, codes_host, x_hat_host)
         return codes_host, x_hat_host

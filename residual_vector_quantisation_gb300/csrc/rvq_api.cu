@@ -24,6 +24,8 @@ rvq_status check_dims(const rvq_dims &dm) {
   if (dm.d != rvq::kCodeDim && dm.d != rvq::kCodeDimSmall) return RVQ_ERR_UNSUPPORTED;
   if (dm.K % 128 != 0 || dm.K > (dm.d == rvq::kCodeDim ? 65536 : rvq::kMaxKSmall)) return RVQ_ERR_UNSUPPORTED;
   if (dm.D % 16 != 0 || dm.D > 16384) return RVQ_ERR_UNSUPPORTED;
+  if (dm.D_in < 0 || dm.D_out < 0) return RVQ_ERR_INVALID_ARG;
+  if (dm.D_in % 16 != 0 || dm.D_in > 16384 || dm.D_out % 16 != 0 || dm.D_out > 16384) return RVQ_ERR_UNSUPPORTED;
   if (dm.Q > rvq::kMaxStages) return RVQ_ERR_UNSUPPORTED;
   return RVQ_OK;
 }
@@ -98,6 +100,10 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
   if (!aligned256(tables) || !aligned16(weights->w_in) || !aligned16(weights->codebook) ||
       !aligned16(weights->w_out))
     return RVQ_ERR_INVALID_ARG;
+  // frames of another width need fc; an output of another width needs fc2
+  if (!weights->fc_w && rvq::dim_in(dims) != dims.D) return RVQ_ERR_INVALID_ARG;
+  if (!weights->fc2_w && rvq::dim_out(dims) != dims.D) return RVQ_ERR_INVALID_ARG;
+  if ((weights->fc_b && !weights->fc_w) || (weights->fc2_b && !weights->fc2_w)) return RVQ_ERR_INVALID_ARG;
   if (tables_bytes < rvq::tables_layout(dims).total) return RVQ_ERR_INVALID_ARG;
   return launch_status(rvq::launch_prepare(dims, *weights, tables, reinterpret_cast<cudaStream_t>(stream)));
 }

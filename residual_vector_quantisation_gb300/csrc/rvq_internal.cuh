@@ -25,35 +25,44 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 __host__ __device__ inline int64_t n_pairs(int Q) { return (int64_t)Q * (Q - 1) / 2; }
 __host__ __device__ inline int64_t pair_index(int q, int s) { return (int64_t)q * (q - 1) / 2 + s; }
 
+// Widths of encode's frames and decode's output (D without fc / fc2).
+inline int dim_in(const rvq_dims &dm) { return dm.D_in > 0 ? dm.D_in : dm.D; }
+inline int dim_out(const rvq_dims &dm) { return dm.D_out > 0 ? dm.D_out : dm.D; }
+
 // Byte offsets of the prepared tables inside the caller's tables buffer.
 struct TablesLayout {
-  size_t w_in_hi;  // [Q*d][D]  f32, TF32-truncated high part
-  size_t w_in_lo;  // [Q*d][D]  f32, w_in - w_in_hi (exact)
+  size_t w_in_hi;  // [Q*d][D_in]  f32, TF32-truncated high part of w_in (. fc_w)
+  size_t w_in_lo;  // [Q*d][D_in]  f32, the exact remainder
   size_t b_in;     // [Q*d]     f32 (zeros when absent)
   size_t cnorm;    // [Q][K]    f32 squared norms (float64 sums)
   size_t cb_img;   // [Q][K/128][hi,lo][2][128 x 32] f32: -2*codebook split in TF32 hi/lo,
                    //   each 128-codeword chunk as two 128-byte-swizzled K-major atoms
-  size_t z;        // [Q][K][D] f32 decode table
+  size_t z;        // [Q][K][D_out] f32 decode table (fc2 folded in)
+  size_t b_dec;    // [D_out]   f32 decode bias (fc2_b, zeros without fc2)
   size_t g;        // [P][K][d] f32 cross-stage table, P = Q(Q-1)/2
   size_t m64;      // [P][d][d] f64 w_in[q] . w_out[s]   (prepare temporary)
   size_t vb64;     // [P][d]    f64 w_in[q] . b_out[s]   (prepare temporary)
+  size_t m2_64;    // [Q][D_out][d] f64 fc2_w . w_out[q], then [Q][D_out] fc2_w . b_out[q]  (prepare temporary)
   size_t total;
 };
 
 inline TablesLayout tables_layout(const rvq_dims &dm) {
-  const size_t D = dm.D, d = dm.d, K = dm.K, Q = dm.Q, P = (size_t)n_pairs(dm.Q);
+  const size_t d = dm.d, K = dm.K, Q = dm.Q, P = (size_t)n_pairs(dm.Q);
+  const size_t Di = dim_in(dm), Do = dim_out(dm);
   TablesLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
-  L.w_in_hi = take(Q * d * D * 4);
-  L.w_in_lo = take(Q * d * D * 4);
+  L.w_in_hi = take(Q * d * Di * 4);
+  L.w_in_lo = take(Q * d * Di * 4);
   L.b_in = take(Q * d * 4);
   L.cnorm = take(Q * K * 4);
   L.cb_img = take(Q * K * d * 2 * 4);
-  L.z = take(Q * K * D * 4);
+  L.z = take(Q * K * Do * 4);
+  L.b_dec = take(Do * 4);
   L.g = take((P ? P : 1) * K * d * 4);
   L.m64 = take((P ? P : 1) * d * d * 8);
   L.vb64 = take((P ? P : 1) * d * 8);
+  L.m2_64 = take(Q * Do * (d + 1) * 8);
   L.total = o;
   return L;
 }

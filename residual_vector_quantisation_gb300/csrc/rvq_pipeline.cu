@@ -21,8 +21,8 @@ SlotLayout slot_layout(const rvq_dims &dm, int32_t n_q, int64_t chunk) {
   SlotLayout s{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = rvq::align_up(o + bytes); return at; };
-  s.x = take((size_t)chunk * dm.D * sizeof(float));
-  s.y = take((size_t)chunk * dm.D * sizeof(float));
+  s.x = take((size_t)chunk * rvq::dim_in(dm) * sizeof(float));
+  s.y = take((size_t)chunk * rvq::dim_out(dm) * sizeof(float));
   s.codes = take((size_t)chunk * n_q * sizeof(int32_t));
   s.scratch_bytes = rvq::kScratchHeader + (size_t)chunk * n_q * dm.d * sizeof(float);
   s.scratch = take(s.scratch_bytes);
@@ -129,7 +129,8 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *p, const void *tables,
     bool ok = true;
     // slot reuse: the copy-out of chunk i - kSlots has finished with this slot
     if (i >= kSlots) ok = ok && cudaStreamWaitEvent(p->s_in, p->ev_out[slot], 0) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(x_d, x_host + n0 * dm.D, (size_t)n * dm.D * sizeof(float), cudaMemcpyHostToDevice,
+    const int64_t Di = rvq::dim_in(dm), Do = rvq::dim_out(dm);
+    ok = ok && cudaMemcpyAsync(x_d, x_host + n0 * Di, (size_t)n * Di * sizeof(float), cudaMemcpyHostToDevice,
                                p->s_in) == cudaSuccess;
     ok = ok && cudaEventRecord(p->ev_in[slot], p->s_in) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(p->s_comp, p->ev_in[slot], 0) == cudaSuccess;
@@ -145,7 +146,7 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *p, const void *tables,
     ok = ok && cudaMemcpyAsync(codes_host + n0 * n_q, c_d, (size_t)n * n_q * sizeof(int32_t), cudaMemcpyDeviceToHost,
                                p->s_out) == cudaSuccess;
     if (x_hat_host)
-      ok = ok && cudaMemcpyAsync(x_hat_host + n0 * dm.D, y_d, (size_t)n * dm.D * sizeof(float),
+      ok = ok && cudaMemcpyAsync(x_hat_host + n0 * Do, y_d, (size_t)n * Do * sizeof(float),
                                  cudaMemcpyDeviceToHost, p->s_out) == cudaSuccess;
     ok = ok && cudaEventRecord(p->ev_out[slot], p->s_out) == cudaSuccess;
     if (!ok) status = RVQ_ERR_CUDA;

@@ -9,6 +9,12 @@
 //   Z[q][k]       = w_out[q] . codebook[q][k] + b_out[q]         (decode table)
 //   G[q][s][k]    = w_in[q] . Z[s][k]            for s < q      (cross-stage table)
 //
+// With the codec's Linear layers (omnivoice.cpp ARCHITECTURE.md, "Audio
+// tokenizer": fc before the RVQ encode, fc2 after the RVQ decode):
+//   w_in'[q] = w_in[q] . fc_w,  b_in'[q] = w_in[q] . fc_b + b_in[q]   (projection of raw frames)
+//   Z'[q][k] = fc2_w . Z[q][k]  (so the decode table is D_out wide), decode bias fc2_b
+// while G stays in the quantizer's own space.
+//
 // Z re-associates the decode graph of omnivoice.cpp ARCHITECTURE.md ("RVQ
 // codec": gather, project_out, add bias, accumulate) into one gather per
 // stage.  G re-associates the encode loop of the same section: since
@@ -45,6 +51,64 @@ __device__ __forceinline__ double codeword_divisor(const float *c, int d, int me
   double s = 0.0;
   for (int j = 0; j < d; ++j) s += (double)c[j] * (double)c[j];
   return fmax(sqrt(s), 1e-12);
+}
+
+// w_in' = w_in . fc_w (float64 sums), split into TF32 hi / lo, and
+// b_in' = w_in . fc_b + b_in.  grid: (Q*d, ceil(D_in/256)); 256 threads.
+__global__ void __launch_bounds__(256) k_prep_w_in_fc(const float *__restrict__ w_in, const float *__restrict__ b_in,
+                                                      const float *__restrict__ fc_w, const float *__restrict__ fc_b,
+                                                      float *__restrict__ hi, float *__restrict__ lo,
+                                                      float *__restrict__ b_in_out, int D, int D_in) {
+  const int64_t r = blockIdx.x;  // row q*d + j
+  const int i = blockIdx.y * blockDim.x + threadIdx.x;
+  const float *wr = w_in + r * D;
+  if (i < D_in) {
+    double s = 0.0;
+    for (int m = 0; m < D; ++m) s += (double)wr[m] * (double)fc_w[(int64_t)m * D_in + i];
+    const float v = (float)s;
+    const float h = tf32_trunc(v);
+    hi[r * D_in + i] = h;
+    lo[r * D_in + i] = v - h;
+  }
+  if (blockIdx.y == 0 && threadIdx.x < 32) {  // the bias, one warp
+    double s = 0.0;
+    if (fc_b)
+      for (int m = threadIdx.x; m < D; m += 32) s += (double)wr[m] * (double)fc_b[m];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) b_in_out[r] = (float)(s + (b_in ? (double)b_in[r] : 0.0));
+  }
+}
+
+// fc2 folded into the stage outputs: M2[q][o][j] = sum_i fc2_w[o][i] w_out[q][i][j],
+// v2[q][o] = sum_i fc2_w[o][i] b_out[q][i] (float64).  grid: (Q, D_out); block: d + 32.
+template <int d>
+__global__ void k_prep_m2(const float *__restrict__ fc2_w, const float *__restrict__ w_out,
+                          const float *__restrict__ b_out, double *__restrict__ m2, double *__restrict__ v2, int D,
+                          int D_out) {
+  const int q = blockIdx.x, o = blockIdx.y;
+  const float *fr = fc2_w + (int64_t)o * D;
+  constexpr int kJThreads = (d + 31) / 32 * 32;
+  if (threadIdx.x < kJThreads) {
+    const int j = threadIdx.x;
+    if (j >= d) return;
+    const float *wo = w_out + (int64_t)q * D * d + j;
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) acc += (double)fr[i] * (double)wo[(int64_t)i * d];
+    m2[((int64_t)q * D_out + o) * d + j] = acc;
+  } else {
+    const int lane = threadIdx.x - kJThreads;  // one whole warp
+    double acc = 0.0;
+    if (b_out)
+      for (int i = lane; i < D; i += 32) acc += (double)fr[i] * (double)b_out[(int64_t)q * D + i];
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) v2[(int64_t)q * D_out + o] = acc;
+  }
+}
+
+// The decode bias: fc2_b, or zeros.
+__global__ void k_prep_b_dec(const float *__restrict__ fc2_b, float *__restrict__ b_dec, int D_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < D_out) b_dec[i] = fc2_b ? fc2_b[i] : 0.0f;
 }
 
 // Squared norms of the codewords as the distance uses them (float64 sums).
@@ -103,11 +167,12 @@ __global__ void k_prep_cb_img8(const float *__restrict__ cb, float *__restrict__
   img[(chunk + 1) * (128 * d) + off] = lo;
 }
 
-// Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64).
+// Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64);
+// with fc2 the same with M2, v2 of width D_out for w_out, b_out.
 // grid: (ceil(D/256), Q*K/16); each block handles 16 codewords of one stage.
-template <int d>
-__global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
-                                                const float *__restrict__ b_out,
+template <int d, class TW>
+__global__ void __launch_bounds__(256) k_prep_z(const TW *__restrict__ w_out,
+                                                const TW *__restrict__ b_out,
                                                 const float *__restrict__ cb, float *__restrict__ z,
                                                 int D, int K) {
   __shared__ double sc[16][d];
@@ -118,7 +183,7 @@ __global__ void __launch_bounds__(256) k_prep_z(const float *__restrict__ w_out,
   __syncthreads();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= D) return;
-  const float *wr = w_out + ((int64_t)q * D + i) * d;
+  const TW *wr = w_out + ((int64_t)q * D + i) * d;
   double w[d];
 #pragma unroll
   for (int j = 0; j < d; ++j) w[j] = (double)wr[j];
@@ -197,8 +262,18 @@ void launch_tables(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaS
   const TablesLayout L = tables_layout(dm);
   const int D = dm.D, K = dm.K, Q = dm.Q;
   const int64_t rows = (int64_t)Q * K, P = n_pairs(Q);
-  k_prep_z<d><<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
-                                                                             at<float>(tables, L.z), D, K);
+  const int D_out = dim_out(dm);
+  if (w.fc2_w) {
+    double *m2 = at<double>(tables, L.m2_64), *v2 = m2 + (size_t)Q * D_out * d;
+    k_prep_m2<d><<<dim3((unsigned)Q, (unsigned)D_out), (d + 31) / 32 * 32 + 32, 0, st>>>(w.fc2_w, w.w_out, w.b_out, m2,
+                                                                                         v2, D, D_out);
+    k_prep_z<d, double><<<dim3((D_out + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(
+        m2, v2, w.codebook, at<float>(tables, L.z), D_out, K);
+  } else {
+    k_prep_z<d, float><<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
+                                                                                     at<float>(tables, L.z), D, K);
+  }
+  k_prep_b_dec<<<(D_out + 255) / 256, 256, 0, st>>>(w.fc2_b, at<float>(tables, L.b_dec), D_out);
   if (P > 0) {
     k_prep_m<d><<<dim3((unsigned)P, d), (d + 31) / 32 * 32 + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
                                                          at<double>(tables, L.vb64), D, Q);
@@ -210,9 +285,16 @@ void launch_tables(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaS
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t st) {
   const TablesLayout L = tables_layout(dm);
   const int D = dm.D, d = dm.d, K = dm.K, Q = dm.Q;
-  const int64_t nw = (int64_t)Q * d * D;
-  k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
-                                   at<float>(tables, L.b_in), nw, (int64_t)Q * d);
+  if (w.fc_w) {
+    const int D_in = dim_in(dm);
+    k_prep_w_in_fc<<<dim3((unsigned)(Q * d), (unsigned)((D_in + 255) / 256)), 256, 0, st>>>(
+        w.w_in, w.b_in, w.fc_w, w.fc_b, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
+        at<float>(tables, L.b_in), D, D_in);
+  } else {
+    const int64_t nw = (int64_t)Q * d * D;
+    k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
+                                     at<float>(tables, L.b_in), nw, (int64_t)Q * d);
+  }
   const int64_t rows = (int64_t)Q * K;
   k_prep_cnorm<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cnorm), d, rows,
                                                                dm.metric);

@@ -60,6 +60,7 @@ MASK64 = (1 << 64) - 1
 
 # Tensor identifiers inside one seed.
 T_W_IN, T_CODEBOOK, T_W_OUT, T_CODES, T_X, T_B_IN, T_B_OUT = 1, 2, 3, 4, 5, 6, 7
+T_FC_W, T_FC_B, T_FC2_W, T_FC2_B = 8, 9, 10, 11
 
 BASE_SEED = 20261202
 
@@ -78,6 +79,16 @@ class Workload:
     cb_decay: float = 1.0
     seed: int = BASE_SEED
     metric: str = "l2"   # "l2" | "cosine" (argmin between L2-normalised vectors)
+    fc_in: int = 0       # with an fc Linear layer (fc_in -> D) before the quantizer: its input width
+    fc_out: int = 0      # with an fc2 Linear layer (D -> fc_out) after decode: its output width
+
+    @property
+    def D_in(self) -> int:
+        return self.fc_in or self.D
+
+    @property
+    def D_out(self) -> int:
+        return self.fc_out or self.D
 
     @property
     def N(self) -> int:
@@ -86,7 +97,9 @@ class Workload:
     def describe(self) -> str:
         return (f"{self.name}: B={self.B} T={self.T} N={self.N} D={self.D} Q={self.Q} "
                 f"K={self.K} d={self.d} kind={self.kind} sigma={self.sigma} "
-                f"cb_decay={self.cb_decay} seed={self.seed} metric={self.metric}")
+                f"cb_decay={self.cb_decay} seed={self.seed} metric={self.metric}"
+                + (f" fc={self.fc_in}->{self.D}" if self.fc_in else "")
+                + (f" fc2={self.D}->{self.fc_out}" if self.fc_out else ""))
 
 
 WORKLOADS = [
@@ -102,6 +115,10 @@ WORKLOADS = [
     # L2-normalised vectors in an 8-dim code space (moss-tts.cpp AGENTS.md,
     # gotchas 9 and 12); the latent size is not given there, D=768 as moss_deep
     Workload("moss_lfq", 32, 375, 768, 32, 1024, 8, "gauss", cb_decay=0.8, seed=BASE_SEED + 6, metric="cosine"),
+    # the OmniVoice codec with the Linear layers around its quantizer
+    # (omnivoice.cpp ARCHITECTURE.md, "Audio tokenizer": fc 1024 -> 1024 before
+    # the RVQ encode, fc2 1024 -> 256 after the RVQ decode)
+    Workload("omnivoice_fc", 16, 750, 1024, 8, 1024, 64, "gauss", seed=BASE_SEED + 7, fc_in=1024, fc_out=256),
 ]
 WORKLOAD_BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -185,6 +202,14 @@ def make_weights(w: Workload, with_bias: bool = False, bias_scale: float = 0.1) 
     if with_bias:
         out["b_in"] = (bias_scale * _gauss_block(w.seed, T_B_IN, 0, Q * d)).reshape(Q, d).astype(np.float32)
         out["b_out"] = (bias_scale * _gauss_block(w.seed, T_B_OUT, 0, Q * D)).reshape(Q, D).astype(np.float32)
+    if w.fc_in:   # fc: weight [D][D_in] ~ N(0, 1/D_in), bias N(0, 0.1^2)
+        out["fc_w"] = (_gauss_block(w.seed, T_FC_W, 0, D * w.fc_in) / math.sqrt(w.fc_in)).reshape(D, w.fc_in) \
+            .astype(np.float32)
+        out["fc_b"] = (0.1 * _gauss_block(w.seed, T_FC_B, 0, D)).astype(np.float32)
+    if w.fc_out:  # fc2: weight [D_out][D] ~ N(0, 1/D), bias N(0, 0.1^2)
+        out["fc2_w"] = (_gauss_block(w.seed, T_FC2_W, 0, w.fc_out * D) / math.sqrt(D)).reshape(w.fc_out, D) \
+            .astype(np.float32)
+        out["fc2_b"] = (0.1 * _gauss_block(w.seed, T_FC2_B, 0, w.fc_out)).astype(np.float32)
     return out
 
 
@@ -197,15 +222,17 @@ def make_codes(w: Workload, rows: Optional[np.ndarray] = None) -> np.ndarray:
 
 def make_x(w: Workload, weights: dict, rows: Optional[np.ndarray] = None,
            chunk: int = 8192) -> np.ndarray:
-    """Frames x [len(rows)][D] float32 on the CPU.
+    """Frames x [len(rows)][D_in] float32 on the CPU (D_in = D without fc).
 
     gauss:   x ~ N(0, 1)
     planted: x = sum_q w_out[q] @ codebook[q][c_q] + sigma * g   (float64, rounded once)
     """
     if w.kind == "decode":
         raise ValueError("decode-only workload has no frames")
+    if w.kind == "planted" and w.fc_in:
+        raise ValueError("planted frames live in the quantizer's space: no fc")
     rows = np.arange(w.N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
-    D = w.D
+    D = w.D_in
     out = np.empty((len(rows), D), dtype=np.float32)
     key = stream_key(w.seed, T_X)
     if w.kind == "planted":
@@ -293,7 +320,9 @@ def make_x_torch(w: Workload, weights_dev: dict, device, chunk: int = 16384):
     import torch
     if w.kind == "decode":
         raise ValueError("decode-only workload has no frames")
-    D = w.D
+    if w.kind == "planted" and w.fc_in:
+        raise ValueError("planted frames live in the quantizer's space: no fc")
+    D = w.D_in
     out = torch.empty((w.N, D), dtype=torch.float32, device=device)
     key = stream_key(w.seed, T_X)
     ar = torch.arange(D, dtype=torch.int64, device=device)

@@ -57,6 +57,14 @@ def test_early_return_paths(lib_path):
     assert lib.rvq_dims_supported(rq.rvq_dims(768, 16, 1024, 32)) == -2  # d neither 8 nor 64
     assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 8, 2)) == -1  # unknown metric
     assert lib.rvq_tables_bytes(rq.rvq_dims(768, 8, 1024, 32, 1)) > 0
+    # frame and output widths of the codec's Linear layers
+    assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 8, 0, 1024, 256)) == 0
+    assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 8, 0, 1000, 256)) == -2   # D_in % 16
+    assert lib.rvq_dims_supported(rq.rvq_dims(1024, 64, 1024, 8, 0, 0, -16)) == -1
+    w = rq.rvq_weights(1 << 20, None, 1 << 20, 1 << 20, None, None, None, None, None)
+    fake = ctypes.c_void_p(1 << 20)
+    # D_in != D without fc_w is rejected before any launch
+    assert lib.rvq_prepare(rq.rvq_dims(1024, 64, 1024, 8, 0, 512, 0), ctypes.byref(w), fake, 1 << 40, None) == -1
     assert lib.rvq_tables_bytes(ok) > 8 * 1024 * 1024 * 4                # holds Z at least
     assert lib.rvq_encode_min_scratch_bytes(ok, 8) == 256 + 128 * 8 * 64 * 4
     assert lib.rvq_encode_scratch_bytes(ok, 100, 8) == 256 + 100 * 8 * 64 * 4

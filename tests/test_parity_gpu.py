@@ -34,7 +34,8 @@ def _lib():
 
 def make_rvq(W, metric="l2"):
     t = ri.weights_to_torch(W, DEV)
-    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV, metric=metric)
+    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV, metric=metric,
+                  fc_w=t.get("fc_w"), fc_b=t.get("fc_b"), fc2_w=t.get("fc2_w"), fc2_b=t.get("fc2_b"))
 
 
 def check_encode(W, x, codes_gpu, rows=None, n_q=None, x_rms=None, x_hat_gpu=None, label="", metric="l2"):
@@ -345,3 +346,53 @@ def test_cosine_d64_workload_shapes():
         w, W = _small_weights(D=256, K=K, Q=4, seed=N % 97, d=64)
         x = np.random.default_rng(N).standard_normal((N, 256)).astype(np.float32)
         run_small(W, x, label=f"cosine d=64 N={N} K={K}", metric="cosine")
+
+
+# ---------------------------------------------------------------------------
+# the codec's Linear layers folded into the tables (fc before, fc2 after)
+# ---------------------------------------------------------------------------
+
+def _with_fc(W, D, D_in, D_out, seed):
+    rng = np.random.default_rng(seed)
+    W = dict(W)
+    if D_in:
+        W["fc_w"] = (rng.standard_normal((D, D_in)) / np.sqrt(D_in)).astype(np.float32)
+        W["fc_b"] = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    if D_out:
+        W["fc2_w"] = (rng.standard_normal((D_out, D)) / np.sqrt(D)).astype(np.float32)
+        W["fc2_b"] = (0.1 * rng.standard_normal(D_out)).astype(np.float32)
+    return W
+
+
+@pytest.mark.parametrize("D,D_in,D_out,d,metric", [(128, 96, 64, 64, "l2"), (128, 256, 0, 64, "cosine"),
+                                                   (96, 0, 32, 8, "cosine"), (64, 64, 64, 8, "l2")])
+def test_fc_and_fc2_folded(D, D_in, D_out, d, metric):
+    """fc (D_in -> D) folded into the projections and fc2 (D -> D_out) into the
+    decode table, against the oracle applying both explicitly in float64."""
+    w, W = _small_weights(D=D, K=256, Q=4, seed=D + D_in + D_out + d, d=d)
+    W = _with_fc(W, D, D_in, D_out, seed=d + D_in)
+    x = np.random.default_rng(D_in + 1).standard_normal((700, D_in or D)).astype(np.float32)
+    rvq = make_rvq(W, metric)
+    codes, x_hat = rvq.reconstruct(torch.from_numpy(x).to(DEV))
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    y_ref, _ = oracle.decode(W, c)
+    assert x_hat.shape == (700, D_out or D)
+    check_encode(W, x, c, x_rms=rms(y_ref), x_hat_gpu=x_hat.cpu().numpy(), label=f"fc {D_in}->{D}->{D_out}",
+                 metric=metric)
+
+
+def test_omnivoice_fc_workload_sampled():
+    """The OmniVoice codec shape with fc 1024 -> 1024 and fc2 1024 -> 256:
+    2000 sampled frames checked on the oracle."""
+    w = ri.WORKLOAD_BY_NAME["omnivoice_fc"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)
+    rvq = make_rvq(W, w.metric)
+    codes, x_hat = rvq.reconstruct(torch.from_numpy(x).to(DEV))
+    torch.cuda.synchronize()
+    rows = np.sort(np.concatenate([np.random.default_rng(4).choice(w.N - 2, 1998, replace=False) + 1, [0, w.N - 1]]))
+    c = codes.cpu().numpy()
+    y_ref, _ = oracle.decode(W, c[rows])
+    res = check_encode(W, x, c, rows=rows, x_rms=rms(y_ref), x_hat_gpu=x_hat.cpu().numpy(), label="omnivoice_fc")
+    assert res["n_equal"] >= 0.97 * res["n_stages"]
