@@ -249,6 +249,22 @@ RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const fl
                                      int64_t n_frames, int32_t n_q, int32_t *codes,
                                      rvq_stream_t stream);
 
+/* Small batches.  A call of at most `max_frames` frames (rvq_encode,
+ * rvq_reconstruct, rvq_encode_static, and each chunk of a larger call) runs on
+ * a low-latency kernel: each group of up to 16 frames is spread over one
+ * cluster of min(8, K/128) CTAs that each own a slice of every codebook and
+ * exchange their best (distance, index) per frame through distributed shared
+ * memory, so a call of a few frames finishes in microseconds instead of
+ * walking every codeword of every stage on one SM.  It computes the same
+ * codes (distances in float32 FMA; ties to the lowest index) and takes
+ * d = 8 (any n_q), or d = 64 with K <= 4096 and at most as many stages as its
+ * shared memory holds (n_q <= 44 for K <= 1024, 31 for K = 2048, 15 for
+ * K = 4096); other shapes use the tile kernels.  Sets the process-wide threshold (0 turns the small-batch kernel
+ * off) and returns the previous one; a negative argument only returns the
+ * current value.  The default is 64 frames.  Thread-safe; a change applies to
+ * calls made after it. */
+RVQ_API int64_t rvq_set_stream_max_frames(int64_t max_frames);
+
 /* Static strings. */
 RVQ_API const char *rvq_status_string(rvq_status status);
 RVQ_API const char *rvq_version(void);

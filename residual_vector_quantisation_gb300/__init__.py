@@ -30,7 +30,7 @@ __all__ = [
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "RVQ_STATIC_SCRATCH_BYTES", "RVQ",
     "EXPORTED_SYMBOLS", "rvq_pipeline_workspace_bytes", "rvq_pipeline_create", "rvq_pipeline_destroy",
-    "rvq_pipeline_reconstruct", "RVQPipeline",
+    "rvq_pipeline_reconstruct", "RVQPipeline", "rvq_set_stream_max_frames",
 ]
 
 RVQ_OK = 0
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = [
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "rvq_pipeline_workspace_bytes",
-    "rvq_pipeline_create", "rvq_pipeline_destroy", "rvq_pipeline_reconstruct",
+    "rvq_pipeline_create", "rvq_pipeline_destroy", "rvq_pipeline_reconstruct", "rvq_set_stream_max_frames",
 ]
 
 RVQ_STATIC_SCRATCH_BYTES = 16 << 20  # include/rvq.h
@@ -103,6 +103,7 @@ def load_library(path: Optional[str] = None):
         "rvq_pipeline_create": ([rvq_dims, i32, i64, vp, sz, ctypes.POINTER(vp)], ctypes.c_int),
         "rvq_pipeline_destroy": ([vp], ctypes.c_int),
         "rvq_pipeline_reconstruct": ([vp, vp, vp, i64, vp, vp], ctypes.c_int),
+        "rvq_set_stream_max_frames": ([i64], i64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -229,6 +230,11 @@ def rvq_status_string(status: int) -> str:
 
 def rvq_version() -> str:
     return load_library().rvq_version().decode()
+
+
+def rvq_set_stream_max_frames(max_frames: int) -> int:
+    """Threshold (frames per call) of the small-batch kernel; returns the previous one."""
+    return int(load_library().rvq_set_stream_max_frames(int(max_frames)))
 
 
 # ---------------------------------------------------------------------------

@@ -168,6 +168,6 @@ RVQ_API const char *rvq_status_string(rvq_status status) {
   return "unknown status";
 }
 
-RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.2.0 (sm_103a)"; }
+RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.3.0 (sm_103a)"; }
 
 }  // extern "C"

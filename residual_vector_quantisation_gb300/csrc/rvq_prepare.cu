@@ -105,6 +105,38 @@ __global__ void k_prep_m2(const float *__restrict__ fc2_w, const float *__restri
   }
 }
 
+// The streaming path's tables: w_in' transposed to [q][i][j] (hi + lo, exact),
+// and the codebook (normalised for the cosine metric) cut into CS slices of
+// kc = K/CS codewords, each slice stored [j/4][kk] in float4 units.
+__global__ void k_prep_w_in_t(const float *__restrict__ hi, const float *__restrict__ lo, float *__restrict__ wt,
+                              int d, int D_in, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*D_in*d, output order
+  if (e >= n) return;
+  const int j = (int)(e % d);
+  const int64_t qi = e / d;
+  const int i = (int)(qi % D_in);
+  const int64_t q = qi / D_in;
+  const int64_t src = (q * d + j) * D_in + i;
+  wt[e] = hi[src] + lo[src];
+}
+
+__global__ void k_prep_cb_stream(const float *__restrict__ cb, float *__restrict__ out, int d, int K, int CS,
+                                 int64_t n, int metric) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*K*d, output order
+  if (e >= n) return;
+  const int kc = K / CS, n4 = d / 4;
+  const int c = (int)(e % 4);
+  int64_t r = e / 4;
+  const int kk = (int)(r % kc);
+  r /= kc;
+  const int jb = (int)(r % n4);
+  r /= n4;
+  const int rank = (int)(r % CS);
+  const int64_t q = r / CS;
+  const int64_t row = q * K + (int64_t)rank * kc + kk;
+  out[e] = (float)((double)cb[row * d + 4 * jb + c] / codeword_divisor(cb + row * d, d, metric));
+}
+
 // The decode bias: fc2_b, or zeros.
 __global__ void k_prep_b_dec(const float *__restrict__ fc2_b, float *__restrict__ b_dec, int D_out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -294,6 +326,15 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
     const int64_t nw = (int64_t)Q * d * D;
     k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
                                      at<float>(tables, L.b_in), nw, (int64_t)Q * d);
+  }
+  {  // the streaming path's copies: w_in' transposed, the plain (normalised) codebook
+    const int D_in = dim_in(dm);
+    const int64_t nt = (int64_t)Q * D_in * d, nc = (int64_t)Q * K * d;
+    k_prep_w_in_t<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(at<float>(tables, L.w_in_hi),
+                                                                  at<float>(tables, L.w_in_lo),
+                                                                  at<float>(tables, L.w_in_t), d, D_in, nt);
+    k_prep_cb_stream<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_stream), d, K,
+                                                                     stream_cluster_size(K), nc, dm.metric);
   }
   const int64_t rows = (int64_t)Q * K;
   k_prep_cnorm<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cnorm), d, rows,

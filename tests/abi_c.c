@@ -52,6 +52,14 @@ int main(void) {
   EXPECT(strcmp(rvq_status_string(RVQ_OK), "ok") == 0);
   EXPECT(rvq_status_string(RVQ_ERR_CUDA) != NULL);
   EXPECT(rvq_version() != NULL && strlen(rvq_version()) > 0);
+  {
+    const int64_t prev = rvq_set_stream_max_frames(-1); /* query only */
+    EXPECT(prev >= 0);
+    EXPECT(rvq_set_stream_max_frames(5) == prev);
+    EXPECT(rvq_set_stream_max_frames(-1) == 5);
+    EXPECT(rvq_set_stream_max_frames(prev) == 5);
+    EXPECT(rvq_set_stream_max_frames(-7) == prev);
+  }
   if (failures == 0) printf("abi_c: ok\n");
   return failures == 0 ? 0 : 1;
 }

@@ -172,10 +172,17 @@ def _small_weights(D=64, K=256, Q=4, seed=3, bias=False, decay=1.0, d=64):
 
 
 @pytest.mark.parametrize("N", [1, 2, 63, 64, 65, 127, 129, 333])
-def test_ragged_frame_counts(N):
+@pytest.mark.parametrize("threshold", [0, None])
+def test_ragged_frame_counts(N, threshold):
+    """threshold 0: the tile kernels even for a single frame; None: the default
+    split (small calls on the streaming kernel)."""
     w, W = _small_weights(D=128, K=256, Q=3, seed=10 + N)
     x = np.random.default_rng(N).standard_normal((N, 128)).astype(np.float32)
-    run_small(W, x, label=f"N={N}")
+    prev = rq.rvq_set_stream_max_frames(-1 if threshold is None else threshold)
+    try:
+        run_small(W, x, label=f"N={N}")
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
 
 
 @pytest.mark.parametrize("D,K,Q", [(16, 128, 1), (48, 128, 2), (256, 384, 5), (2048, 256, 2),

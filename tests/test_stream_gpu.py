@@ -1,0 +1,251 @@
+"""The small-batch (streaming) encode kernel against the float64 oracle.
+
+Calls of at most rvq_set_stream_max_frames frames run on the cluster kernel
+(each 16-frame group on one cluster of min(8, K/128) CTAs that exchange their
+best keys through distributed shared memory).  These tests raise the
+threshold so that every call of the shapes below takes it, compare every
+frame with the oracle under the near-tie rule, and check the reconstruction
+through decode.  Shapes cover every cluster size (K = 128 .. 1024), the wide
+slices (K = 2048, 4096), both metrics, d = 8 and 64, biases, prefix depths,
+stage counts that are not multiples of the cluster size, ragged frame counts
+(1, 2, 7, 16, 17, 33, 64, 300) and the workload shapes.
+"""
+
+import contextlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rvq_inputs as ri
+from rvq_compare import FLOAT_TOL, compare_codes, max_abs_rel_to_rms, rms
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import residual_vector_quantisation_gb300 as rq  # noqa: E402
+from residual_vector_quantisation_gb300 import build as rqb  # noqa: E402
+
+DEV = torch.device("cuda:0")
+ALL = 1 << 40  # threshold that sends every call to the streaming kernel
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rqb.build_library()
+    rq.load_library()
+    prev = rq.rvq_set_stream_max_frames(-1)
+    yield
+    rq.rvq_set_stream_max_frames(prev)
+
+
+@contextlib.contextmanager
+def stream_max(frames):
+    prev = rq.rvq_set_stream_max_frames(frames)
+    try:
+        yield
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
+
+
+def make_rvq(W, metric="l2"):
+    t = ri.weights_to_torch(W, DEV)
+    return rq.RVQ(t["w_in"], t["codebook"], t["w_out"], t["b_in"], t["b_out"], device=DEV, metric=metric,
+                  fc_w=t.get("fc_w"), fc_b=t.get("fc_b"), fc2_w=t.get("fc2_w"), fc2_b=t.get("fc2_b"))
+
+
+def weights(D, K, Q, d, seed, bias=True, decay=1.0):
+    w = ri.Workload("stream", 1, 1, D, Q, K, d, "gauss", cb_decay=decay, seed=seed)
+    return ri.make_weights(w, with_bias=bias, bias_scale=0.3)
+
+
+def check(W, x, n_q=None, metric="l2", label="", threshold=ALL):
+    """Encode + reconstruct on the streaming kernel; every frame against the oracle."""
+    rvq = make_rvq(W, metric)
+    xt = torch.from_numpy(x).to(DEV)
+    with stream_max(threshold):
+        codes, x_hat = rvq.reconstruct(xt, n_q)
+        codes_e = rvq.encode(xt, n_q)
+    torch.cuda.synchronize()
+    c = codes.cpu().numpy()
+    assert np.array_equal(c, codes_e.cpu().numpy()), f"{label}: encode and reconstruct disagree"
+    ref = oracle.encode(W, x, n_q, want_residual=False, metric=metric)
+    res = compare_codes(c, ref["codes"], ref["gap"])
+    assert res["n_fail"] == 0, f"{label}: code mismatches at clear decisions: {res}"
+    y_ref, _ = oracle.decode(W, c, c.shape[1])
+    err = max_abs_rel_to_rms(x_hat.cpu().numpy(), y_ref, max(rms(y_ref), 1e-30))
+    assert err <= FLOAT_TOL, f"{label}: x_hat error {err:.3e} * RMS"
+    return res, c
+
+
+@pytest.mark.parametrize("N", [1, 2, 7, 16, 17, 33, 64])
+@pytest.mark.parametrize("K", [128, 256, 512, 1024])
+def test_cluster_sizes_and_ragged_counts(N, K):
+    """Cluster sizes 1, 2, 4, 8 (K/128 CTAs up to 8) and frame counts that leave
+    the last 16-frame group partly empty."""
+    D, Q = 128, 5
+    W = weights(D, K, Q, 64, seed=K + N)
+    x = np.random.default_rng(N * 7 + K).standard_normal((N, D)).astype(np.float32)
+    check(W, x, label=f"N={N} K={K}")
+
+
+@pytest.mark.parametrize("K,Q", [(2048, 3), (4096, 10)])
+def test_wide_slices(K, Q):
+    """256 and 512 codewords per CTA (one thread per codeword, the second with
+    one slice buffer instead of two)."""
+    D = 256
+    W = weights(D, K, Q, 64, seed=K)
+    x = np.random.default_rng(K).standard_normal((40, D)).astype(np.float32)
+    check(W, x, label=f"K={K}")
+
+
+@pytest.mark.parametrize("d,K,Q,metric", [(64, 1024, 8, "cosine"), (64, 256, 11, "cosine"), (8, 1024, 32, "cosine"),
+                                          (8, 128, 3, "l2"), (8, 512, 9, "l2"), (8, 1024, 12, "cosine")])
+def test_metrics_and_code_dims(d, K, Q, metric):
+    D = 96
+    W = weights(D, K, Q, d, seed=d * K + Q, decay=0.8)
+    x = np.random.default_rng(Q).standard_normal((37, D)).astype(np.float32)
+    check(W, x, metric=metric, label=f"d={d} K={K} Q={Q} {metric}")
+
+
+def test_prefix_depths_and_stage_counts():
+    """n_q below Q (the partial-depth encode) gives the prefix of the full codes;
+    stage counts 1 .. 13 against a cluster of 8."""
+    D, K, Q = 192, 1024, 13
+    W = weights(D, K, Q, 64, seed=99)
+    x = np.random.default_rng(3).standard_normal((20, D)).astype(np.float32)
+    _, full = check(W, x, label="full depth")
+    for n_q in (1, 2, 7, 8, 9):
+        _, c = check(W, x, n_q=n_q, label=f"n_q={n_q}")
+        assert np.array_equal(c, full[:, :n_q]), "prefix property"
+
+
+def test_many_groups():
+    """300 frames: 19 clusters of 8 CTAs, some waiting for a free GPC."""
+    D, K, Q = 256, 1024, 8
+    W = weights(D, K, Q, 64, seed=5)
+    x = np.random.default_rng(5).standard_normal((300, D)).astype(np.float32)
+    check(W, x, label="300 frames")
+
+
+@pytest.mark.parametrize("name", ["tiny", "omnivoice", "moss_deep", "k4096_q10", "moss_lfq", "omnivoice_fc"])
+def test_workload_shapes_small_batches(name):
+    """The first frames of each workload, in calls of 1, 16 and 48 frames."""
+    w = ri.WORKLOAD_BY_NAME[name]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)[:48]
+    for n in (1, 16, 48):
+        check(W, np.ascontiguousarray(x[:n]), metric=w.metric, label=f"{name} n={n}")
+
+
+def test_planted_codes_recovered():
+    """Frames built as sums of the stage outputs of chosen codes, with
+    well-separated codebooks and no noise, give back those codes."""
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, w.K, size=(16, w.Q)).astype(np.int32)
+    x, _ = oracle.decode(W, codes)
+    rvq = make_rvq(W)
+    with stream_max(ALL):
+        got = rvq.encode(torch.from_numpy(x.astype(np.float32)).to(DEV)).cpu().numpy()
+    ref = oracle.encode(W, x.astype(np.float32), want_residual=False)
+    res = compare_codes(got, ref["codes"], ref["gap"])
+    assert res["n_fail"] == 0, res
+
+
+def test_exact_ties_take_lowest_index():
+    """Duplicated codewords in different slices (different CTAs of the cluster)
+    and in the same slice: the lower index wins."""
+    D, K, Q = 64, 1024, 2
+    W = weights(D, K, Q, 64, seed=77, bias=False)
+    W["w_in"] = np.stack([np.eye(64, dtype=np.float32)] * Q)
+    W["w_out"] = np.stack([np.eye(64, dtype=np.float32)] * Q)
+    for q in range(Q):
+        for lo, hi in ((3, 900), (17, 18), (300, 1023), (130, 260)):
+            W["codebook"][q, hi] = W["codebook"][q, lo]
+    picks = np.array([3, 900, 17, 18, 300, 1023, 130, 260] * 2)
+    rng = np.random.default_rng(8)
+    x = (W["codebook"][0][picks] + 0.01 * rng.standard_normal((len(picks), D))).astype(np.float32)
+    rvq = make_rvq(W)
+    with stream_max(ALL):
+        codes = rvq.encode(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    ref = oracle.encode(W, x)
+    assert np.array_equal(codes[:, 0], ref["codes"][:, 0])
+    assert set(codes[:, 0].tolist()) <= {3, 17, 300, 130}
+
+
+def test_tile_and_stream_paths_agree():
+    """Both paths on the same frames: each passes the oracle rule, and they give
+    the same code wherever the oracle's decision is clear."""
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    x = ri.make_x(w, W)[:64]
+    rvq = make_rvq(W)
+    xt = torch.from_numpy(x).to(DEV)
+    with stream_max(0):
+        c_tile = rvq.encode(xt).cpu().numpy()
+    with stream_max(ALL):
+        c_stream = rvq.encode(xt).cpu().numpy()
+    ref = oracle.encode(W, x, want_residual=False)
+    for c in (c_tile, c_stream):
+        assert compare_codes(c, ref["codes"], ref["gap"])["n_fail"] == 0
+    assert (c_tile == c_stream).mean() >= 0.99
+
+
+def test_static_entry_point_and_determinism():
+    """rvq_encode_static on small batches takes the same kernel; repeated calls
+    give identical codes."""
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    x = torch.from_numpy(ri.make_x(w, W)[:24]).to(DEV)
+    rvq = make_rvq(W)
+    with stream_max(ALL):
+        a = rvq.encode(x)
+        b = torch.empty_like(a)
+        rq.rvq_encode_static(rvq.dims, rvq.tables, x, w.Q, b)
+        c = rvq.encode(x)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_unsupported_shapes_fall_back():
+    """Shapes the streaming kernel does not take (d = 64 with K > 4096; more
+    stages than its shared memory holds) run on the tile kernels."""
+    for D, K, Q in ((64, 8192, 2), (64, 256, 60)):
+        W = weights(D, K, Q, 64, seed=K + Q)
+        x = np.random.default_rng(K).standard_normal((10, D)).astype(np.float32)
+        check(W, x, label=f"fallback K={K} Q={Q}")
+
+
+def test_the_streaming_kernel_runs():
+    """The kernel list of a small call names the cluster kernel (and of a call
+    with the threshold at 0, only the tile kernels)."""
+    from torch.profiler import ProfilerActivity, profile
+
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    x = torch.from_numpy(ri.make_x(w, W)[:8]).to(DEV)
+    rvq = make_rvq(W)
+    rvq.encode(x)
+    torch.cuda.synchronize()
+
+    def kernels(threshold):
+        with stream_max(threshold), profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+            canary = torch.full((4,), 2.0, device=DEV) * 3.0  # a torch kernel: shows that kernels are traced
+            rvq.encode(x)
+            torch.cuda.synchronize()
+        del canary
+        return [e.name for e in prof.events()]
+
+    ks = kernels(ALL)
+    if not any("elementwise_kernel" in k for k in ks):  # the canary's kernel
+        pytest.skip(f"the profiler traced no kernels here (only {sorted(set(ks))[:6]})")
+    assert any("k_encode_stream" in k for k in ks), ks
+    assert not any("k_search" in k or "k_project" in k for k in ks), ks
+    kt = kernels(0)
+    assert not any("k_encode_stream" in k for k in kt), kt
+    assert any("k_search" in k for k in kt), kt
