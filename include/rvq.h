@@ -251,15 +251,15 @@ RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const fl
 
 /* Small batches.  A call of at most `max_frames` frames (rvq_encode,
  * rvq_reconstruct, rvq_encode_static, and each chunk of a larger call) runs on
- * a low-latency kernel: each group of up to 16 frames is spread over one
- * cluster of min(8, K/128) CTAs that each own a slice of every codebook and
- * exchange their best (distance, index) per frame through distributed shared
- * memory, so a call of a few frames finishes in microseconds instead of
- * walking every codeword of every stage on one SM.  It computes the same
+ * low-latency kernels: the stage projections spread over many CTAs, then
+ * each group of up to 16 frames on one cluster of min(8, K/128) CTAs that
+ * each own a slice of every codebook and exchange their best (distance,
+ * index) per frame through distributed shared memory, so a call of a few
+ * frames finishes in microseconds instead of walking every codeword of every
+ * stage on one SM.  It computes the same
  * codes (distances in float32 FMA; ties to the lowest index) and takes
- * d = 8 (any n_q), or d = 64 with K <= 4096 and at most as many stages as its
- * shared memory holds (n_q <= 44 for K <= 1024, 31 for K = 2048, 15 for
- * K = 4096); other shapes use the tile kernels.  Sets the process-wide threshold (0 turns the small-batch kernel
+ * d = 8, or d = 64 with K <= 4096 (and n_q <= 42 when K = 128); other shapes
+ * use the tile kernels.  Sets the process-wide threshold (0 turns the small-batch kernel
  * off) and returns the previous one; a negative argument only returns the
  * current value.  The default is 64 frames.  Thread-safe; a change applies to
  * calls made after it. */

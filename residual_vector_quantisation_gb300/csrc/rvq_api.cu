@@ -60,6 +60,9 @@ rvq_status encode_impl(const rvq_dims &dm, const void *tables, const float *x, i
   if (chunk < n_frames && chunk >= wave) chunk = chunk / wave * wave;
   int *status = static_cast<int *>(scratch);
   float *p0 = reinterpret_cast<float *>(static_cast<char *>(scratch) + rvq::kScratchHeader);
+  if (chunk >= n_frames && rvq::stream_supported(dm, n_q, n_frames))  // one small batch: its first kernel
+    return launch_status(                                              // clears the status word
+        rvq::launch_encode_stream(dm, tables, x, n_frames, n_q, codes, p0, status, true, st));
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return RVQ_ERR_CUDA;
   for (int64_t n0 = 0; n0 < n_frames; n0 += chunk) {
     const int64_t n = (n_frames - n0 < chunk) ? n_frames - n0 : chunk;

@@ -77,9 +77,13 @@ extern "C" RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *table
   if (static_scratch(&scratch) != cudaSuccess) return RVQ_ERR_CUDA;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int *status = static_cast<int *>(scratch);
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return RVQ_ERR_CUDA;
-  cudaError_t e = rvq::launch_encode_chunk(
-      dims, tables, x, 0, n_frames, n_q, codes,
-      reinterpret_cast<float *>(static_cast<char *>(scratch) + rvq::kScratchHeader), status, st);
+  float *p0 = reinterpret_cast<float *>(static_cast<char *>(scratch) + rvq::kScratchHeader);
+  cudaError_t e;
+  if (rvq::stream_supported(dims, n_q, n_frames)) {  // its first kernel clears the status word
+    e = rvq::launch_encode_stream(dims, tables, x, n_frames, n_q, codes, p0, status, true, st);
+  } else {
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return RVQ_ERR_CUDA;
+    e = rvq::launch_encode_chunk(dims, tables, x, 0, n_frames, n_q, codes, p0, status, st);
+  }
   return e == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA;
 }

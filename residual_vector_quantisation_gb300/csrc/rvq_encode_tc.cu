@@ -845,8 +845,8 @@ int sm_count() {
 
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0, int64_t n,
                                 int n_q, int32_t *codes, float *p0, int *status, cudaStream_t st) {
-  if (stream_supported(dm, n_q, n))  // a small batch: the low-latency cluster kernel
-    return launch_encode_stream(dm, tables, x + n0 * dim_in(dm), n, n_q, codes + n0 * n_q, status, st);
+  if (stream_supported(dm, n_q, n))  // a small batch: the low-latency cluster kernels
+    return launch_encode_stream(dm, tables, x + n0 * dim_in(dm), n, n_q, codes + n0 * n_q, p0, status, false, st);
   const TablesLayout L = tables_layout(dm);
   const int D = dim_in(dm), d = dm.d, K = dm.K, Q = dm.Q;  // frames are D_in wide (fc folded into w_in)
   const int n_cols = n_q * d;

@@ -43,7 +43,7 @@ struct TablesLayout {
   size_t m64;      // [P][d][d] f64 w_in[q] . w_out[s]   (prepare temporary)
   size_t vb64;     // [P][d]    f64 w_in[q] . b_out[s]   (prepare temporary)
   size_t m2_64;    // [Q][D_out][d] f64 fc2_w . w_out[q], then [Q][D_out] fc2_w . b_out[q]  (prepare temporary)
-  size_t w_in_t;   // [Q][D_in][d] f32 w_in (. fc_w) transposed: the streaming path's projection
+  size_t w_in_f;   // [Q*d][D_in] f32 w_in (. fc_w) (hi + lo): the streaming path's projection
   size_t cb_stream;  // [Q][CS][d/4][K/CS] float4: the codebook (each codeword divided by n(c) for the
                      //   cosine metric) cut into the streaming path's CS = stream_cluster_size(K) slices,
                      //   each slice column-block major so one bulk copy stages it
@@ -67,7 +67,7 @@ inline TablesLayout tables_layout(const rvq_dims &dm) {
   L.m64 = take((P ? P : 1) * d * d * 8);
   L.vb64 = take((P ? P : 1) * d * 8);
   L.m2_64 = take(Q * Do * (d + 1) * 8);
-  L.w_in_t = take(Q * Di * d * 4);
+  L.w_in_f = take(Q * d * Di * 4);
   L.cb_stream = take(Q * K * d * 4);
   L.total = o;
   return L;
@@ -92,8 +92,10 @@ constexpr int kStreamFrames = 16;
 constexpr int kStreamMaxFramesDefault = 64;
 __host__ __device__ inline int stream_cluster_size(int K) { return K / 128 < 8 ? K / 128 : 8; }
 bool stream_supported(const rvq_dims &dm, int n_q, int64_t n_frames);
+// p0: scratch for the stage projections ([n][n_q*d] f32); zero_status: the
+// first kernel clears the status word (the caller has not).
 cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q,
-                                 int32_t *codes, int *status, cudaStream_t s);
+                                 int32_t *codes, float *p0, int *status, bool zero_status, cudaStream_t s);
 cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q,
                            int32_t *codes, int *status, int sms, cudaStream_t s);
 cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t *codes, int64_t n,

@@ -105,19 +105,13 @@ __global__ void k_prep_m2(const float *__restrict__ fc2_w, const float *__restri
   }
 }
 
-// The streaming path's tables: w_in' transposed to [q][i][j] (hi + lo, exact),
-// and the codebook (normalised for the cosine metric) cut into CS slices of
-// kc = K/CS codewords, each slice stored [j/4][kk] in float4 units.
-__global__ void k_prep_w_in_t(const float *__restrict__ hi, const float *__restrict__ lo, float *__restrict__ wt,
-                              int d, int D_in, int64_t n) {
-  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q*D_in*d, output order
-  if (e >= n) return;
-  const int j = (int)(e % d);
-  const int64_t qi = e / d;
-  const int i = (int)(qi % D_in);
-  const int64_t q = qi / D_in;
-  const int64_t src = (q * d + j) * D_in + i;
-  wt[e] = hi[src] + lo[src];
+// The streaming path's tables: w_in' in float32 (hi + lo, exact), and the
+// codebook (normalised for the cosine metric) cut into CS slices of kc = K/CS
+// codewords, each slice stored [j/4][kk] in float4 units.
+__global__ void k_prep_w_in_f(const float *__restrict__ hi, const float *__restrict__ lo, float *__restrict__ wf,
+                              int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < n) wf[e] = hi[e] + lo[e];
 }
 
 __global__ void k_prep_cb_stream(const float *__restrict__ cb, float *__restrict__ out, int d, int K, int CS,
@@ -327,12 +321,12 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
     k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
                                      at<float>(tables, L.b_in), nw, (int64_t)Q * d);
   }
-  {  // the streaming path's copies: w_in' transposed, the plain (normalised) codebook
+  {  // the streaming path's copies: w_in' in float32, the sliced (normalised) codebook
     const int D_in = dim_in(dm);
     const int64_t nt = (int64_t)Q * D_in * d, nc = (int64_t)Q * K * d;
-    k_prep_w_in_t<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(at<float>(tables, L.w_in_hi),
+    k_prep_w_in_f<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(at<float>(tables, L.w_in_hi),
                                                                   at<float>(tables, L.w_in_lo),
-                                                                  at<float>(tables, L.w_in_t), d, D_in, nt);
+                                                                  at<float>(tables, L.w_in_f), nt);
     k_prep_cb_stream<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_stream), d, K,
                                                                      stream_cluster_size(K), nc, dm.metric);
   }

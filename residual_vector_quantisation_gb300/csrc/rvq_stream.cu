@@ -5,31 +5,37 @@
 // soon as the first sentence is complete, and moss-tts.cpp AGENTS.md has a
 // realtime TTS front end.  For such calls the tile path (128-frame tiles, one
 // CTA per tile walking all K codewords of every stage) leaves the GPU idle
-// and its latency is the serial walk over Q*K codewords.  Here each group of
-// up to 16 frames runs on one thread-block cluster of CS = min(8, K/128) CTAs,
-// CTA r owning codewords [r*kc, (r+1)*kc), kc = K/CS, of every stage:
+// and its latency is the serial walk over Q*K codewords.  Here:
 //
-//   projection  CTA r computes P0[q] = w_in'[q] . x + b_in'[q] for its stages
-//               q = r, r+CS, ... (float32 FMA, the sum over D_in split over
-//               thread groups) and stores it into the shared memory of every
-//               CTA of the cluster; a cluster barrier publishes them.
-//   stage q     each CTA scores its slice (staged in shared memory by a bulk
-//               copy issued NB stages ahead) against the frames' p_q:
-//               dist = ||c||^2 - 2 s p.c  (s = 1, or 1/max(||p||, 1e-12) for
-//               the cosine metric), keeping per frame the minimum of the key
-//               (distance, index); the CS keys of each frame are exchanged
-//               through distributed shared memory (remote stores, then one
-//               release-arrive per source on the destination's mbarrier); the
-//               smallest key is the code -- distance first, then the lowest
-//               index, as the plain argmin of the pages.
-//   update      p_{q+1} -= G[q+1][q][code_q] right after the exchange (the
-//               cross-stage table of rvq_prepare); the terms for later stages
-//               are applied while the next exchange is in flight.
+//   k_project_small   P0[n][q*d + j] = w_in'[q][j] . x[n] + b_in'[q][j] for
+//                     every stage, spread over (n_q*d/8) x ceil(n/16) CTAs
+//                     (8 output columns and 16 frames each; frames and weight
+//                     rows staged in shared memory by bulk copies, float32
+//                     FMA).  It lets the next kernel launch at once
+//                     (programmatic dependent launch).
+//   k_stream_search   each group of up to 16 frames on one thread-block
+//                     cluster of CS = min(8, K/128) CTAs.  CTA r owns
+//                     codewords [r*kc, (r+1)*kc), kc = K/CS, of every stage
+//                     (staged in shared memory by a bulk copy NB stages ahead)
+//                     and the projections of stages q = r (mod CS).  Stage q:
+//       distances     dist = ||c||^2 - 2 s p.c for the CTA's slice (s = 1, or
+//                     1/max(||p||, 1e-12) for the cosine metric), float32 FMA;
+//                     per frame the minimum of the key (distance, index);
+//       exchange      the CS keys of each frame go to every CTA by st.async
+//                     into its shared memory, counted by an mbarrier's
+//                     transaction bytes; the smallest key is the code --
+//                     distance first, then the lowest index, as the plain
+//                     argmin of the pages;
+//       update        p_{q+1} -= G[q+1][q][code_q] in every CTA (the
+//                     cross-stage table of rvq_prepare).  The owner of stage
+//                     q+2 applies the same term for it and pushes that stage's
+//                     projection (every term but the last) into every CTA,
+//                     one stage ahead of its use; owners apply the terms of
+//                     later stages to their own copies only.
 //
-// The distances are float32 FMA dot products on the CUDA cores, not tensor
-// core tiles: with at most 16 frames a stage is a [kc x d] by [d x 16] product
-// per CTA, far below one tcgen05 tile, and the path is bound by the exchange
-// and gather latencies, not by arithmetic.
+// The distances run on the CUDA cores, not tensor core tiles: with at most 16
+// frames a stage is a [kc x d] by [d x 16] product per CTA, far below one
+// tcgen05 tile, and the path is bound by latency, not arithmetic.
 //
 // Every mbarrier wait is bounded: a timeout records RVQ_DEVICE_TIMEOUT in the
 // status word and the kernel carries on (codes are clamped to [0, K), so no
@@ -44,16 +50,121 @@ namespace {
 
 using namespace ptx;
 
+__device__ __forceinline__ void st_error(int *status, int code) { atomicCAS(status, 0, code); }
+
+// ===========================================================================
+// k_project_small
+// ===========================================================================
+constexpr int PS_THREADS = 256;
+constexpr int PS_COLS = 8;   // output columns (rows of w_in') per CTA
+constexpr int PS_F = 16;     // frames per CTA
+constexpr int PS_DC = 512;   // D_in elements per staged chunk
+constexpr size_t PS_SMEM = (size_t)2 * (PS_F + PS_COLS) * PS_DC * 4 + 16;
+
+// x [n][D_in], w_f [n_cols][D_in], b_in [n_cols], P0 [n][n_cols].
+// grid (n_cols/8, ceil(n/16)).  Warp w: columns 2(w%4), 2(w%4)+1 of the CTA's
+// 8 and frames 8(w/4) .. +7; lane l: elements 4l + 128m of each chunk.
+__global__ void __launch_bounds__(PS_THREADS)
+    k_project_small(const float *__restrict__ x, const float *__restrict__ w_f, const float *__restrict__ b_in,
+                    float *__restrict__ P0, int64_t n, int D_in, int n_cols, int *__restrict__ status,
+                    int zero_status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  float *xs = reinterpret_cast<float *>(smem);   // [2][PS_F][PS_DC]
+  float *ws = xs + 2 * PS_F * PS_DC;             // [2][PS_COLS][PS_DC]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(ws + 2 * PS_COLS * PS_DC);
+  griddep_launch_dependents();  // the search kernel may start its prologue
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int c0 = blockIdx.x * PS_COLS;
+  const int64_t f0 = (int64_t)blockIdx.y * PS_F;
+  const int nf = (int)(n - f0 < PS_F ? n - f0 : PS_F);
+  if (zero_status && blockIdx.x == 0 && blockIdx.y == 0 && t == 0) *status = 0;
+  if (t == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int nch = (D_in + PS_DC - 1) / PS_DC;
+  auto issue = [&](int c) {  // warp 0: chunk c into buffer c & 1
+    const int b = c & 1, i0 = c * PS_DC;
+    const uint32_t bytes = (uint32_t)((D_in - i0 < PS_DC ? D_in - i0 : PS_DC) * 4);
+    if (c >= 2) fence_proxy_async_smem();  // the buffer's last reads were generic loads
+    if (lane == 0) mbar_arrive_expect_tx(&bar[b], bytes * (uint32_t)(nf + PS_COLS));
+    __syncwarp();
+    if (lane < nf)
+      bulk_g2s(xs + (b * PS_F + lane) * PS_DC, x + (f0 + lane) * (int64_t)D_in + i0, bytes, &bar[b]);
+    else if (lane >= 16 && lane < 16 + PS_COLS)
+      bulk_g2s(ws + (b * PS_COLS + lane - 16) * PS_DC, w_f + (int64_t)(c0 + lane - 16) * D_in + i0, bytes,
+               &bar[b]);
+  };
+  if (warp == 0) {
+    issue(0);
+    if (nch > 1) issue(1);
+  }
+  const int cp = warp & 3, fh = warp >> 2;
+  const bool active = 8 * fh < nf;
+  float acc[2][8] = {};
+  for (int c = 0; c < nch; ++c) {
+    const int b = c & 1;
+    if (!mbar_wait(&bar[b], (uint32_t)((c >> 1) & 1))) st_error(status, RVQ_DEVICE_TIMEOUT);
+    const int len = D_in - c * PS_DC < PS_DC ? D_in - c * PS_DC : PS_DC;
+    if (active) {
+      const float4 *w0 = reinterpret_cast<const float4 *>(ws + (b * PS_COLS + 2 * cp) * PS_DC);
+      const float4 *w1 = w0 + PS_DC / 4;
+      const float4 *xb = reinterpret_cast<const float4 *>(xs + (b * PS_F + 8 * fh) * PS_DC);
+      for (int i4 = lane; 4 * i4 < len; i4 += 32) {
+        const float4 a = w0[i4], e = w1[i4];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 xv = xb[v * (PS_DC / 4) + i4];
+          acc[0][v] = fmaf(xv.x, a.x, acc[0][v]);
+          acc[0][v] = fmaf(xv.y, a.y, acc[0][v]);
+          acc[0][v] = fmaf(xv.z, a.z, acc[0][v]);
+          acc[0][v] = fmaf(xv.w, a.w, acc[0][v]);
+          acc[1][v] = fmaf(xv.x, e.x, acc[1][v]);
+          acc[1][v] = fmaf(xv.y, e.y, acc[1][v]);
+          acc[1][v] = fmaf(xv.z, e.z, acc[1][v]);
+          acc[1][v] = fmaf(xv.w, e.w, acc[1][v]);
+        }
+      }
+    }
+    __syncthreads();  // buffer b is free
+    if (warp == 0 && c + 2 < nch) issue(c + 2);
+  }
+  if (active) {
+#pragma unroll
+    for (int col = 0; col < 2; ++col)
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[col][v] += __shfl_xor_sync(0xffffffffu, acc[col][v], o);
+    if (lane < 16) {
+      const int col = lane >> 3, v = lane & 7, f = 8 * fh + v;
+      float s = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int vv = 0; vv < 8; ++vv)
+          if (cc == col && vv == v) s = acc[cc][vv];
+      const int jc = c0 + 2 * cp + col;
+      if (f < nf) P0[(f0 + f) * n_cols + jc] = s + __ldg(b_in + jc);
+    }
+  }
+}
+
+// ===========================================================================
+// k_stream_search
+// ===========================================================================
 constexpr int ST_THREADS = 256;
-constexpr int ST_F = kStreamFrames;            // frames per cluster
-constexpr int ST_MAX_CS = 8;                    // cluster size limit (portable)
-constexpr uint32_t ST_SMEM_LIMIT = 232448;      // opt-in dynamic shared memory per block
-constexpr int ST_BATCH = 8;                     // table rows in flight per thread in the deferred update
+constexpr int ST_F = kStreamFrames;        // frames per cluster
+constexpr int ST_MAX_CS = 8;                // cluster size limit (portable)
+constexpr uint32_t ST_SMEM_LIMIT = 232448;  // opt-in dynamic shared memory per block
+constexpr int ST_BATCH = 8;                 // table rows in flight per thread in the owners' updates
 
 // Dynamic shared memory layout (byte offsets), the same on host and device.
 struct StreamShape {
-  int CS, kc, NB, slots;
-  uint32_t p, cbuf, cnb, red, xch, loc, cs, sv, bars, total;
+  int CS, kc, NB, slots, n_own;
+  uint32_t pown, pin, cbuf, cnb, red, xch, loc, sv, bars, total;
 };
 
 __host__ __device__ inline uint32_t up16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -63,19 +174,20 @@ __host__ __device__ inline StreamShape stream_shape(int d, int K, int n_q, int N
   S.CS = stream_cluster_size(K);
   S.kc = K / S.CS;
   S.NB = NB;
-  S.slots = S.kc == 128 ? 128 : 256;  // key-writing threads per frame
+  S.slots = S.kc == 128 ? 128 : 256;       // key-writing threads per frame
+  S.n_own = (n_q + S.CS - 1) / S.CS;       // stages owned by rank 0 (the most)
+  const uint32_t row = (uint32_t)ST_F * d * 4;
   uint32_t o = 0;
-  S.p = o;    o = up16(o + (uint32_t)n_q * ST_F * d * 4);                 // [n_q][F][d] stage projections
+  S.pown = o; o = up16(o + (uint32_t)S.n_own * row);                     // [n_own][F][d] owned stages
+  S.pin = o;  o = up16(o + 2u * row);                                    // [2][F][d] pushed stages
   o = (o + 127u) & ~127u;
-  S.cbuf = o; o = up16(o + (uint32_t)NB * S.kc * d * 4);                  // [NB][d/4][kc] float4 slices
-  S.cnb = o;  o = up16(o + (uint32_t)NB * S.kc * 4);                      // [NB][kc] squared norms
-  const uint32_t red_keys = (uint32_t)ST_F * S.slots * 8, red_proj = ST_THREADS * 16 * 4;
-  S.red = o;  o = up16(o + (red_keys > red_proj ? red_keys : red_proj));  // keys / projection partials
-  S.xch = o;  o = up16(o + 2u * ST_MAX_CS * ST_F * 8);                   // [2][rank][F] exchanged keys
-  S.loc = o;  o = up16(o + ST_F * 8);                                     // [F] this CTA's best keys
-  S.cs = o;   o = up16(o + 2u * ST_F * 4);                                // [2][F] codes of the last stages
-  S.sv = o;   o = up16(o + ST_F * 4);                                     // [F] distance scale s
-  S.bars = o; o = up16(o + 4u * 8);                                       // cb_full[2], x_full[2]
+  S.cbuf = o; o = up16(o + (uint32_t)NB * S.kc * d * 4);                 // [NB][d/4][kc] float4 slices
+  S.cnb = o;  o = up16(o + (uint32_t)NB * S.kc * 4);                     // [NB][kc] squared norms
+  S.red = o;  o = up16(o + (uint32_t)ST_F * S.slots * 8);                // [F][slots] keys
+  S.xch = o;  o = up16(o + 2u * ST_MAX_CS * ST_F * 8);                  // [2][rank][F] exchanged keys
+  S.loc = o;  o = up16(o + ST_F * 8);                                    // [F] this CTA's best keys
+  S.sv = o;   o = up16(o + ST_F * 4);                                    // [F] distance scale s
+  S.bars = o; o = up16(o + 6u * 8);                                      // cb_full[2] x_full[2] p_full[2]
   S.total = o;
   return S;
 }
@@ -86,8 +198,6 @@ int stream_nb(int d, int K, int n_q) {
   if (stream_shape(d, K, n_q, 1).total <= ST_SMEM_LIMIT) return 1;
   return 0;
 }
-
-__device__ __forceinline__ void st_error(int *status, int code) { atomicCAS(status, 0, code); }
 
 // Order key of (distance, index): smaller distance first, then lower index.
 // The float is mapped to an unsigned integer of the same order (-0 taken as
@@ -108,128 +218,114 @@ __device__ __forceinline__ void sub4(float4 &p, const float4 g) {
   p.w -= g.w;
 }
 
-// x [n][D_in] (frames of this call), codes [n][n_q].  grid: CS * ceil(n/16)
+__device__ __forceinline__ uint4 as_u4(const float4 v) {
+  return make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+}
+
+// P0 [n][n_q*d] (k_project_small), codes [n][n_q].  grid: CS * ceil(n/16)
 // CTAs in clusters of CS; ST_THREADS threads.  SPLITJ: threads per codeword
-// (2 when kc == 128, each taking every other float4 column).
-template <int d, int SPLITJ>
+// (2 when kc == 128, each taking every other float4 column); NF: frames per
+// cluster computed (16, or fewer when the whole call has fewer).
+template <int d, int SPLITJ, int NF>
 __global__ void __launch_bounds__(ST_THREADS, 1)
-    k_encode_stream(const float *__restrict__ x, const float4 *__restrict__ w_t, const float4 *__restrict__ b_in,
-                    const float4 *__restrict__ cb_s, const float *__restrict__ cnorm, const float4 *__restrict__ g,
-                    int32_t *__restrict__ codes, int64_t n, int D_in, int K, int n_q, int NB, int metric,
-                    int *__restrict__ status) {
+    k_stream_search(const float *__restrict__ P0, const float4 *__restrict__ cb_s, const float *__restrict__ cnorm,
+                    const float4 *__restrict__ g, int32_t *__restrict__ codes, int64_t n, int K, int n_q, int NB,
+                    int metric, int *__restrict__ status) {
   constexpr int TPF = d / 4;            // float4 columns of a row of d
   constexpr int DJ4 = TPF / SPLITJ;     // float4 columns of a codeword per thread
+  constexpr int NU = (NF + 1) / 2;      // 16-byte units of NF keys
+  // lanes of warp 0 taking part when only the first NF*TPF threads work
+  constexpr unsigned kRowMask = NF * TPF >= 32 ? 0xffffffffu : (1u << (NF * TPF)) - 1u;
+  constexpr unsigned kRedMask = 16 * NF >= 32 ? 0xffffffffu : 0x0000ffffu;
   extern __shared__ __align__(128) unsigned char smem[];
   const StreamShape S = stream_shape(d, K, n_q, NB);
   const int t = threadIdx.x;
   const int CS = S.CS, kc = S.kc;
   if (cluster_nctarank() != (uint32_t)CS || blockDim.x != ST_THREADS || dynamic_smem_size() < S.total ||
-      (SPLITJ == 2) != (kc == 128) || (NB != 1 && NB != 2)) {
+      (SPLITJ == 2) != (kc == 128) || (NB != 1 && NB != 2) || (NF < ST_F && n > NF)) {
+    griddep_wait();  // after the projection kernel, which may clear the status word
     if (t == 0) st_error(status, RVQ_DEVICE_BAD_LAUNCH);
     return;  // uniform over the cluster: no CTA reaches a cluster barrier
   }
   const uint32_t rank = cluster_ctarank();
   const int64_t f0 = (int64_t)(blockIdx.x / CS) * ST_F;
   const int nf = (int)(n - f0 < ST_F ? n - f0 : ST_F);
+  const int n_cols = n_q * d;
 
-  float4 *P = reinterpret_cast<float4 *>(smem + S.p);          // [n_q][F][TPF]
-  float4 *cbuf = reinterpret_cast<float4 *>(smem + S.cbuf);    // [NB][TPF][kc]
-  float *cnb = reinterpret_cast<float *>(smem + S.cnb);        // [NB][kc]
-  uint64_t *red = reinterpret_cast<uint64_t *>(smem + S.red);  // [F][slots]
-  uint64_t *xch = reinterpret_cast<uint64_t *>(smem + S.xch);  // [2][ST_MAX_CS][F]
-  uint64_t *loc = reinterpret_cast<uint64_t *>(smem + S.loc);  // [F]
-  int *csm = reinterpret_cast<int *>(smem + S.cs);             // [2][F]
-  float *sv = reinterpret_cast<float *>(smem + S.sv);          // [F]
+  float4 *Pown = reinterpret_cast<float4 *>(smem + S.pown);   // [n_own][F][TPF]
+  float4 *Pin = reinterpret_cast<float4 *>(smem + S.pin);     // [2][F][TPF]
+  float4 *cbuf = reinterpret_cast<float4 *>(smem + S.cbuf);   // [NB][TPF][kc]
+  float *cnb = reinterpret_cast<float *>(smem + S.cnb);       // [NB][kc]
+  uint64_t *red = reinterpret_cast<uint64_t *>(smem + S.red); // [F][slots]
+  uint64_t *xch = reinterpret_cast<uint64_t *>(smem + S.xch); // [2][ST_MAX_CS][F]
+  uint64_t *loc = reinterpret_cast<uint64_t *>(smem + S.loc); // [F]
+  float *sv = reinterpret_cast<float *>(smem + S.sv);         // [F]
   uint64_t *cb_full = reinterpret_cast<uint64_t *>(smem + S.bars);
-  uint64_t *x_full = cb_full + 2;
+  uint64_t *x_full = cb_full + 2, *p_full = cb_full + 4;
 
   const uint32_t slice_bytes = (uint32_t)kc * d * 4, norm_bytes = (uint32_t)kc * 4;
+  // transaction bytes of one exchange (keys from the other CS-1 CTAs) and of
+  // one push (a stage projection from its owner, unless this CTA owns it)
+  const uint32_t x_bytes = (uint32_t)(CS - 1) * NU * 16;
+  auto p_bytes = [&](int q) { return q % CS == (int)rank ? 0u : (uint32_t)NF * TPF * 16; };
   auto issue = [&](int q, int b) {  // one thread: stage q's slice into buffer b
     mbar_arrive_expect_tx(&cb_full[b], slice_bytes + norm_bytes);
     bulk_g2s(cbuf + (size_t)b * TPF * kc, cb_s + ((int64_t)q * CS + rank) * TPF * kc, slice_bytes, &cb_full[b]);
     bulk_g2s(cnb + (size_t)b * kc, cnorm + (int64_t)q * K + (int64_t)rank * kc, norm_bytes, &cb_full[b]);
   };
+  // push one float4 of stage q's projection (frame f, column j4) into every
+  // CTA (this one by a plain store: the same thread reads it back)
+  auto push = [&](int q, int f, int j4, const float4 v) {
+    float4 *slot = Pin + ((q & 1) * ST_F + f) * TPF + j4;
+    const uint32_t dst = smem_addr(slot), bar = smem_addr(&p_full[q & 1]);
+    for (int r = 0; r < CS; ++r)
+      if (r != (int)rank) st_async_u4(cluster_map(dst, (uint32_t)r), as_u4(v), cluster_map(bar, (uint32_t)r));
+    *slot = v;
+  };
 
   if (t == 0) {
     for (int b = 0; b < NB; ++b) mbar_init(&cb_full[b], 1);
-    mbar_init(&x_full[0], (uint32_t)CS);
-    mbar_init(&x_full[1], (uint32_t)CS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&x_full[b], 1);
+      mbar_init(&p_full[b], 1);
+    }
     fence_mbar_init();
+    // this CTA's own arrival for the exchanges and pushes of stages 0 and 1
+    for (int q = 0; q < 2 && q < n_q; ++q) {
+      mbar_arrive_expect_tx(&x_full[q], x_bytes);
+      mbar_arrive_expect_tx(&p_full[q], p_bytes(q));
+    }
   }
   if (t < ST_F) sv[t] = 1.0f;
   __syncthreads();
-  cluster_arrive();  // barriers initialised; waited for before the first remote access
+  cluster_arrive();  // barriers armed; waited for before the first remote access
   if (t == 32)
     for (int q = 0; q < NB && q < n_q; ++q) issue(q, q);
 
-  // ---- projection of this CTA's stages, stored into every CTA's P ----------
-  {
-    const int nfe = nf <= 4 ? 4 : (nf <= 8 ? 8 : 16);  // frames computed, whole blocks of 4
-    const int TG = (nfe / 4) * TPF;                    // threads per slice of D_in
-    const int KG = ST_THREADS / TG;                    // slices of D_in
-    const int gi = t / TG, tg = t % TG, fb = tg / TPF, jb = tg % TPF;
-    const float *xr[4];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int f = 4 * fb + v < nf ? 4 * fb + v : nf - 1;  // padding rows repeat a real frame
-      xr[v] = x + (f0 + f) * (int64_t)D_in;
-    }
-    float4 *part = reinterpret_cast<float4 *>(red);  // [KG][nfe][TPF]
-    bool joined = false;
-    for (int q = (int)rank; q < n_q; q += CS) {
-      float acc[4][4] = {};
-      const float4 *wq = w_t + (int64_t)q * D_in * TPF + jb;
-      for (int i = 4 * gi; i < D_in; i += 4 * KG) {
-        float4 xv[4], wv[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) xv[v] = __ldg(reinterpret_cast<const float4 *>(xr[v] + i));
-#pragma unroll
-        for (int u = 0; u < 4; ++u) wv[u] = __ldg(wq + (int64_t)(i + u) * TPF);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const float xs[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[v][0] = fmaf(xs[u], wv[u].x, acc[v][0]);
-            acc[v][1] = fmaf(xs[u], wv[u].y, acc[v][1]);
-            acc[v][2] = fmaf(xs[u], wv[u].z, acc[v][2]);
-            acc[v][3] = fmaf(xs[u], wv[u].w, acc[v][3]);
-          }
-        }
-      }
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        part[(gi * nfe + 4 * fb + v) * TPF + jb] = make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
-      __syncthreads();
-      if (!joined) {
-        cluster_wait();
-        joined = true;
-      }
-      for (int e = t; e < nfe * TPF; e += ST_THREADS) {
-        const int f = e / TPF, j4 = e % TPF;
-        float4 s = __ldg(b_in + q * TPF + j4);
-        for (int k = 0; k < KG; ++k) {
-          const float4 v = part[(k * nfe + f) * TPF + j4];
-          s.x += v.x;
-          s.y += v.y;
-          s.z += v.z;
-          s.w += v.w;
-        }
-        const uint32_t off = smem_addr(P + ((int64_t)q * ST_F + f) * TPF + j4);
-        for (int r = 0; r < CS; ++r) st_cluster_v4(cluster_map(off, (uint32_t)r), s);
-      }
-      __syncthreads();
-    }
-    if (!joined) cluster_wait();
+  // ---- the owned stages' projections (zero rows past the last frame) --------
+  griddep_wait();  // k_project_small has finished; P0 is visible
+  for (int e = t; e < S.n_own * NF * TPF; e += ST_THREADS) {
+    const int i = e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
+    const int q = (int)rank + i * CS;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q < n_q && f < nf) v = __ldg(reinterpret_cast<const float4 *>(P0 + (f0 + f) * n_cols + q * d) + j4);
+    Pown[(i * ST_F + f) * TPF + j4] = v;
   }
-  cluster_sync_all();  // every stage projection is in every CTA
-
-  if (metric == RVQ_METRIC_COSINE && t < ST_F * TPF) {  // s of stage 0
+  __syncthreads();
+  cluster_wait();
+  for (int q = 0; q < 2 && q < n_q; ++q)  // stages 0 and 1 need no cross-stage term before the push
+    if (q % CS == (int)rank && t < NF * TPF) {
+      const int f = t / TPF, j4 = t % TPF;
+      push(q, f, j4, Pown[((q / CS) * ST_F + f) * TPF + j4]);
+    }
+  if (!mbar_wait_cluster_hot(&p_full[0], 0)) st_error(status, RVQ_DEVICE_TIMEOUT);
+  __syncthreads();  // this CTA's own pushes are visible
+  if (metric == RVQ_METRIC_COSINE && t < NF * TPF) {  // s of stage 0
     const int f = t / TPF, j4 = t % TPF;
-    const float4 v = P[f * TPF + j4];
+    const float4 v = Pin[f * TPF + j4];
     float ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
 #pragma unroll
-    for (int o = TPF / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int o = TPF / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(kRowMask, ss, o);
     if (j4 == 0) sv[f] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
   }
   __syncthreads();
@@ -239,53 +335,69 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const int kk0 = SPLITJ == 2 ? (t >> 1) : t;
   for (int q = 0; q < n_q; ++q) {
     const int b = NB == 2 ? (q & 1) : 0;
+    // Re-arm the barriers whose last phase every thread has now seen (stage
+    // q's push, stage q-1's exchange).  Not earlier: an arm that expects no
+    // bytes completes the next phase at once, and a thread still waiting on
+    // the previous phase would then miss it.
+    if (t == 0) {
+      if (q + 2 < n_q) mbar_arrive_expect_tx(&p_full[q & 1], p_bytes(q + 2));
+      if (q >= 1 && q + 1 < n_q) mbar_arrive_expect_tx(&x_full[(q + 1) & 1], x_bytes);
+    }
     if (!mbar_wait(&cb_full[b], (uint32_t)((NB == 2 ? q >> 1 : q) & 1))) st_error(status, RVQ_DEVICE_TIMEOUT);
 
     // distances of this CTA's slice; per frame the smallest key
-    uint64_t best[ST_F];
+    uint64_t best[NF];
 #pragma unroll
-    for (int f = 0; f < ST_F; ++f) best[f] = ~0ull;
+    for (int f = 0; f < NF; ++f) best[f] = ~0ull;
     {
       const float4 *cq = cbuf + (size_t)b * TPF * kc;
       const float *cnq = cnb + (size_t)b * kc;
-      const float4 *pq = P + (int64_t)q * ST_F * TPF;
+      const float4 *pq = Pin + (q & 1) * ST_F * TPF;
       for (int kk = kk0; kk < kc; kk += ST_THREADS / SPLITJ) {
-        float4 c[DJ4];
+        // dot products of the codeword with every frame, its columns taken
+        // CH float4 at a time (in column order) to bound the registers
+        constexpr int CH = DJ4 < 8 ? DJ4 : 8;
+        float a[NF];
 #pragma unroll
-        for (int m = 0; m < DJ4; ++m) c[m] = cq[(m * SPLITJ + h) * kc + kk];
+        for (int f = 0; f < NF; ++f) a[f] = 0.0f;
+#pragma unroll 1
+        for (int m0 = 0; m0 < DJ4; m0 += CH) {
+          float4 c[CH];
+#pragma unroll
+          for (int m = 0; m < CH; ++m) c[m] = cq[((m0 + m) * SPLITJ + h) * kc + kk];
+#pragma unroll
+          for (int f = 0; f < NF; ++f) {
+            const float4 *pf = pq + f * TPF + h;
+#pragma unroll
+            for (int m = 0; m < CH; ++m) {
+              const float4 pv = pf[(m0 + m) * SPLITJ];
+              a[f] = fmaf(c[m].x, pv.x, a[f]);
+              a[f] = fmaf(c[m].y, pv.y, a[f]);
+              a[f] = fmaf(c[m].z, pv.z, a[f]);
+              a[f] = fmaf(c[m].w, pv.w, a[f]);
+            }
+          }
+        }
         const float cn = cnq[kk];
         const uint32_t kg = rank * (uint32_t)kc + (uint32_t)kk;
 #pragma unroll
-        for (int f = 0; f < ST_F; ++f) {
-          if (f < nf) {
-            const float4 *pf = pq + f * TPF + h;
-            float a = 0.0f;
-#pragma unroll
-            for (int m = 0; m < DJ4; ++m) {
-              const float4 pv = pf[m * SPLITJ];
-              a = fmaf(c[m].x, pv.x, a);
-              a = fmaf(c[m].y, pv.y, a);
-              a = fmaf(c[m].z, pv.z, a);
-              a = fmaf(c[m].w, pv.w, a);
-            }
-            if (SPLITJ == 2) a += __shfl_xor_sync(0xffffffffu, a, 1);
-            best[f] = min_u64(best[f], dist_key(fmaf(-2.0f * sv[f], a, cn), kg));
-          }
+        for (int f = 0; f < NF; ++f) {
+          if (SPLITJ == 2) a[f] += __shfl_xor_sync(0xffffffffu, a[f], 1);
+          best[f] = min_u64(best[f], dist_key(fmaf(-2.0f * sv[f], a[f], cn), kg));
         }
       }
     }
     if (SPLITJ == 1 || h == 0) {
 #pragma unroll
-      for (int f = 0; f < ST_F; ++f)
-        if (f < nf) red[f * S.slots + kk0] = best[f];
+      for (int f = 0; f < NF; ++f) red[f * S.slots + kk0] = best[f];
     }
     __syncthreads();
-    {  // 16 threads per frame reduce its slots
+    if (t < 16 * NF) {  // 16 threads per frame reduce its slots
       const int f = t >> 4, sub = t & 15;
       uint64_t k = ~0ull;
       for (int m = sub; m < S.slots; m += 16) k = min_u64(k, red[f * S.slots + m]);
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) k = min_u64(k, __shfl_xor_sync(0xffffffffu, k, o));
+      for (int o = 8; o > 0; o >>= 1) k = min_u64(k, __shfl_xor_sync(kRedMask, k, o, 16));
       if (sub == 0) loc[f] = k;
     }
     __syncthreads();
@@ -293,62 +405,73 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
       fence_proxy_async_smem();
       issue(q + NB, b);
     }
-    if (t < CS) {  // send this CTA's keys to rank t
+    if (t < CS && t != (int)rank) {  // this CTA's keys to rank t (its own stay in loc)
       const uint32_t dst = cluster_map(smem_addr(xch + ((q & 1) * ST_MAX_CS + rank) * ST_F), (uint32_t)t);
+      const uint32_t bar = cluster_map(smem_addr(&x_full[q & 1]), (uint32_t)t);
       const uint4 *l4 = reinterpret_cast<const uint4 *>(loc);
 #pragma unroll
-      for (int i = 0; i < ST_F / 2; ++i) st_cluster_u4(dst + 16u * i, l4[i]);
-      mbar_arrive_cluster(cluster_map(smem_addr(&x_full[q & 1]), (uint32_t)t));
+      for (int i = 0; i < NU; ++i) st_async_u4(dst + 16u * i, l4[i], bar);
     }
 
-    // deferred terms of the previous code: p_{q'} -= G[q'][q-1][code_{q-1}], q' > q
-    if (q >= 1) {
-      const int *cprev = csm + ((q - 1) & 1) * ST_F;
-      const int items = (n_q - q - 1) * ST_F * TPF;
+    // the exchange: the code of every frame
+    if (!mbar_wait_cluster_hot(&x_full[q & 1], (uint32_t)((q >> 1) & 1))) st_error(status, RVQ_DEVICE_TIMEOUT);
+    if (q + 1 < n_q)  // stage q+1's pushed projection
+      if (!mbar_wait_cluster_hot(&p_full[(q + 1) & 1], (uint32_t)(((q + 1) >> 1) & 1)))
+        st_error(status, RVQ_DEVICE_TIMEOUT);
+    const uint64_t *xq = xch + (q & 1) * ST_MAX_CS * ST_F;
+    auto code_of = [&](int f) {
+      uint64_t kb = loc[f];
+      for (int r = 0; r < CS; ++r)
+        if (r != (int)rank) kb = min_u64(kb, xq[r * ST_F + f]);
+      const uint32_t code = (uint32_t)kb;
+      return code < (uint32_t)K ? code : (uint32_t)K - 1;  // (past K only after a timeout)
+    };
+    const bool own2 = q + 2 < n_q && (q + 2) % CS == (int)rank;
+    if (t < NF * TPF) {
+      const int f = t / TPF, j4 = t % TPF;
+      const uint32_t code = code_of(f);
+      if (rank == 0 && j4 == 0 && f < nf) codes[(f0 + f) * n_q + q] = (int32_t)code;
+      float4 g1, g2;
+      if (q + 1 < n_q) g1 = __ldg(g + (pair_index(q + 1, q) * K + code) * TPF + j4);
+      if (own2) g2 = __ldg(g + (pair_index(q + 2, q) * K + code) * TPF + j4);
+      if (q + 1 < n_q) {  // p_{q+1} complete
+        float4 &pv = Pin[(((q + 1) & 1) * ST_F + f) * TPF + j4];
+        sub4(pv, g1);
+        if (metric == RVQ_METRIC_COSINE) {
+          float ss = pv.x * pv.x + pv.y * pv.y + pv.z * pv.z + pv.w * pv.w;
+#pragma unroll
+          for (int o = TPF / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(kRowMask, ss, o);
+          if (j4 == 0) sv[f] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+        }
+      }
+      if (own2) {  // stage q+2 has every term but its last: push it
+        float4 &pv = Pown[(((q + 2) / CS) * ST_F + f) * TPF + j4];
+        sub4(pv, g2);
+        push(q + 2, f, j4, pv);
+      }
+    }
+    {  // this CTA's later stages q' >= q+3 (q' = rank mod CS)
+      const int first = (q + 3 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
+      const int n_later = S.n_own - first;
+      const int items = n_later > 0 ? n_later * NF * TPF : 0;
       for (int e0 = t; e0 < items; e0 += ST_THREADS * ST_BATCH) {
         float4 gv[ST_BATCH];
 #pragma unroll
         for (int u = 0; u < ST_BATCH; ++u) {
           const int e = e0 + u * ST_THREADS;
           if (e < items) {
-            const int m = e / (ST_F * TPF), fj = e % (ST_F * TPF);
-            const int qq = q + 1 + m, f = fj / TPF, j4 = fj % TPF;
-            gv[u] = __ldg(g + (pair_index(qq, q - 1) * K + cprev[f]) * TPF + j4);
+            const int i = first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
+            const int qq = (int)rank + i * CS;
+            if (qq < n_q) gv[u] = __ldg(g + (pair_index(qq, q) * K + code_of(f)) * TPF + j4);
           }
         }
 #pragma unroll
         for (int u = 0; u < ST_BATCH; ++u) {
           const int e = e0 + u * ST_THREADS;
           if (e < items) {
-            const int m = e / (ST_F * TPF), fj = e % (ST_F * TPF);
-            sub4(P[((int64_t)(q + 1 + m) * ST_F) * TPF + fj], gv[u]);
+            const int i = first + e / (NF * TPF), fj = e % (NF * TPF);
+            if ((int)rank + i * CS < n_q) sub4(Pown[i * ST_F * TPF + fj], gv[u]);
           }
-        }
-      }
-    }
-
-    // the exchange: the code of every frame
-    if (!mbar_wait_cluster_hot(&x_full[q & 1], (uint32_t)((q >> 1) & 1))) st_error(status, RVQ_DEVICE_TIMEOUT);
-    if (t < ST_F * TPF) {
-      const int f = t / TPF, j4 = t % TPF;
-      const uint64_t *xs = xch + (q & 1) * ST_MAX_CS * ST_F + f;
-      uint64_t kb = xs[0];
-      for (int r = 1; r < CS; ++r) kb = min_u64(kb, xs[r * ST_F]);
-      uint32_t code = (uint32_t)kb;
-      if (code >= (uint32_t)K) code = (uint32_t)K - 1;  // only after a timeout
-      if (j4 == 0) {
-        csm[(q & 1) * ST_F + f] = (int)code;
-        if (rank == 0 && f < nf) codes[(f0 + f) * n_q + q] = (int32_t)code;
-      }
-      if (q + 1 < n_q) {
-        const float4 gq = __ldg(g + (pair_index(q + 1, q) * K + code) * TPF + j4);
-        float4 &pv = P[((int64_t)(q + 1) * ST_F + f) * TPF + j4];
-        sub4(pv, gq);
-        if (metric == RVQ_METRIC_COSINE) {
-          float ss = pv.x * pv.x + pv.y * pv.y + pv.z * pv.z + pv.w * pv.w;
-#pragma unroll
-          for (int o = TPF / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-          if (j4 == 0) sv[f] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
         }
       }
     }
@@ -370,9 +493,18 @@ std::atomic<unsigned long long> g_stream_attr_done{0};
 std::atomic<int64_t> g_stream_max_frames{kStreamMaxFramesDefault};
 
 template <int d, int SPLITJ>
-cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(k_encode_stream<d, SPLITJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)ST_SMEM_LIMIT);
+cudaError_t set_search_attrs() {
+  cudaError_t e = cudaSuccess;
+  auto set = [&](auto kern) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ST_SMEM_LIMIT);
+  };
+  set(k_stream_search<d, SPLITJ, 1>);
+  set(k_stream_search<d, SPLITJ, 2>);
+  set(k_stream_search<d, SPLITJ, 4>);
+  set(k_stream_search<d, SPLITJ, 8>);
+  set(k_stream_search<d, SPLITJ, 16>);
+  return e;
 }
 
 cudaError_t ensure_stream_attributes() {
@@ -381,11 +513,37 @@ cudaError_t ensure_stream_attributes() {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (g_stream_attr_done.load() & bit) return cudaSuccess;
-  if ((e = set_smem_attr<kCodeDim, 2>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<kCodeDim, 1>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<kCodeDimSmall, 2>()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_project_small, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_SMEM)) !=
+      cudaSuccess)
+    return e;
+  if ((e = set_search_attrs<kCodeDim, 2>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDim, 1>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDimSmall, 2>()) != cudaSuccess) return e;
   g_stream_attr_done.fetch_or(bit);
   return cudaSuccess;
+}
+
+template <int d, int SPLITJ>
+cudaError_t launch_search(cudaLaunchConfig_t &cfg, int nf_max, const float *p0, const float4 *cb_s, const float *cn,
+                          const float4 *g, int32_t *codes, int64_t n, int K, int n_q, int NB, int metric,
+                          int *status) {
+  switch (nf_max) {
+    case 1:
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 1>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
+                                status);
+    case 2:
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 2>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
+                                status);
+    case 4:
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 4>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
+                                status);
+    case 8:
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 8>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
+                                status);
+    default:
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
+                                status);
+  }
 }
 
 }  // namespace
@@ -402,37 +560,40 @@ bool stream_supported(const rvq_dims &dm, int n_q, int64_t n_frames) {
 }
 
 cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q,
-                                 int32_t *codes, int *status, cudaStream_t st) {
+                                 int32_t *codes, float *p0, int *status, bool zero_status, cudaStream_t st) {
   const TablesLayout L = tables_layout(dm);
   cudaError_t e = ensure_stream_attributes();
   if (e != cudaSuccess) return e;
+  const int D_in = dim_in(dm), n_cols = n_q * dm.d;
+  const int64_t groups = (n + ST_F - 1) / ST_F;
+  k_project_small<<<dim3((unsigned)(n_cols / PS_COLS), (unsigned)groups), PS_THREADS, PS_SMEM, st>>>(
+      x, at<float>(tables, L.w_in_f), at<float>(tables, L.b_in), p0, n, D_in, n_cols, status, zero_status ? 1 : 0);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
   const int NB = stream_nb(dm.d, dm.K, n_q);
   const StreamShape S = stream_shape(dm.d, dm.K, n_q, NB);
-  const int64_t clusters = (n + ST_F - 1) / ST_F;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(clusters * S.CS), 1, 1);
+  cfg.gridDim = dim3((unsigned)(groups * S.CS), 1, 1);
   cfg.blockDim = dim3(ST_THREADS, 1, 1);
   cfg.dynamicSmemBytes = S.total;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)S.CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const float4 *w_t = at<float4>(tables, L.w_in_t), *b_in = at<float4>(tables, L.b_in);
+  cfg.numAttrs = 2;
+  const int nf_max = n > 8 ? 16 : n > 4 ? 8 : n > 2 ? 4 : (int)n;  // frames per cluster, >= min(n, 16)
   const float4 *cb_s = at<float4>(tables, L.cb_stream), *g = at<float4>(tables, L.g);
   const float *cn = at<float>(tables, L.cnorm);
-  const int D_in = dim_in(dm);
   if (dm.d == kCodeDimSmall)
-    return cudaLaunchKernelEx(&cfg, k_encode_stream<kCodeDimSmall, 2>, x, w_t, b_in, cb_s, cn, g, codes, n, D_in,
-                              dm.K, n_q, NB, dm.metric, status);
+    return launch_search<kCodeDimSmall, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
   if (S.kc == 128)
-    return cudaLaunchKernelEx(&cfg, k_encode_stream<kCodeDim, 2>, x, w_t, b_in, cb_s, cn, g, codes, n, D_in, dm.K,
-                              n_q, NB, dm.metric, status);
-  return cudaLaunchKernelEx(&cfg, k_encode_stream<kCodeDim, 1>, x, w_t, b_in, cb_s, cn, g, codes, n, D_in, dm.K,
-                            n_q, NB, dm.metric, status);
+    return launch_search<kCodeDim, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+  return launch_search<kCodeDim, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
 }
 
 }  // namespace rvq

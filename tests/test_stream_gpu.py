@@ -57,6 +57,11 @@ def make_rvq(W, metric="l2"):
                   fc_w=t.get("fc_w"), fc_b=t.get("fc_b"), fc2_w=t.get("fc2_w"), fc2_b=t.get("fc2_b"))
 
 
+def device_status(rvq):
+    """The status word at the head of the encode scratch (0: no device wait gave up)."""
+    return int(rvq._scratch[:4].view(torch.int32).item())
+
+
 def weights(D, K, Q, d, seed, bias=True, decay=1.0):
     w = ri.Workload("stream", 1, 1, D, Q, K, d, "gauss", cb_decay=decay, seed=seed)
     return ri.make_weights(w, with_bias=bias, bias_scale=0.3)
@@ -68,8 +73,11 @@ def check(W, x, n_q=None, metric="l2", label="", threshold=ALL):
     xt = torch.from_numpy(x).to(DEV)
     with stream_max(threshold):
         codes, x_hat = rvq.reconstruct(xt, n_q)
+        torch.cuda.synchronize()
+        assert device_status(rvq) == 0, f"{label}: device status word set"
         codes_e = rvq.encode(xt, n_q)
     torch.cuda.synchronize()
+    assert device_status(rvq) == 0, f"{label}: device status word set"
     c = codes.cpu().numpy()
     assert np.array_equal(c, codes_e.cpu().numpy()), f"{label}: encode and reconstruct disagree"
     ref = oracle.encode(W, x, n_q, want_residual=False, metric=metric)
@@ -81,7 +89,7 @@ def check(W, x, n_q=None, metric="l2", label="", threshold=ALL):
     return res, c
 
 
-@pytest.mark.parametrize("N", [1, 2, 7, 16, 17, 33, 64])
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 7, 9, 10, 15, 16, 17, 33, 64])
 @pytest.mark.parametrize("K", [128, 256, 512, 1024])
 def test_cluster_sizes_and_ragged_counts(N, K):
     """Cluster sizes 1, 2, 4, 8 (K/128 CTAs up to 8) and frame counts that leave
@@ -214,8 +222,9 @@ def test_static_entry_point_and_determinism():
 
 def test_unsupported_shapes_fall_back():
     """Shapes the streaming kernel does not take (d = 64 with K > 4096; more
-    stages than its shared memory holds) run on the tile kernels."""
-    for D, K, Q in ((64, 8192, 2), (64, 256, 60)):
+    stages than its shared memory holds) run on the tile kernels; 64 stages
+    with K = 256 (30 owned per CTA) still fit."""
+    for D, K, Q in ((64, 8192, 2), (64, 128, 60), (64, 256, 64)):
         W = weights(D, K, Q, 64, seed=K + Q)
         x = np.random.default_rng(K).standard_normal((10, D)).astype(np.float32)
         check(W, x, label=f"fallback K={K} Q={Q}")
