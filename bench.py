@@ -456,6 +456,62 @@ def per_workload_table(args):
         torch.cuda.empty_cache()
 
 
+def latency_table(args):
+    """Small-batch encode latency for each encode workload: calls of 1, 16 and
+    256 frames on the streaming kernels (the default for calls of up to
+    rvq_set_stream_max_frames frames) and, for comparison, on the tile kernels
+    (threshold 0).  Per call: CUDA-event time of back-to-back calls on one
+    stream, and the median host wall time of a single call with a synchronize
+    (launch overhead included)."""
+    import torch
+    import residual_vector_quantisation_gb300 as rq
+    dev = torch.device("cuda", 0)
+    default = rq.rvq_set_stream_max_frames(-1)
+    only = None if args.workload == WORKLOAD else args.workload  # --workload picks one (profiling)
+    sizes = (args.frames,) if args.frames else (1, 16, 256)
+    for w in ri.WORKLOADS:
+        if w.kind == "decode" or (only and w.name != only):
+            continue
+        W = ri.make_weights(w)
+        Wt = ri.weights_to_torch(W, dev)
+        rvq = rq.RVQ(Wt["w_in"], Wt["codebook"], Wt["w_out"], Wt["b_in"], Wt["b_out"], device=dev, metric=w.metric,
+                     fc_w=Wt.get("fc_w"), fc_b=Wt.get("fc_b"), fc2_w=Wt.get("fc2_w"), fc2_b=Wt.get("fc2_b"))
+        x = torch.from_numpy(ri.make_x(w, W, np.arange(min(w.N, max(sizes))))).to(dev)
+        for n in sizes:
+            if n > x.shape[0]:
+                continue
+            xs = x[:n].contiguous()
+            codes = torch.empty((n, w.Q), dtype=torch.int32, device=dev)
+            scratch = rvq.scratch_for(n, w.Q)
+            row = {"workload": w.name, "frames": n, "Q": w.Q, "K": w.K, "d": w.d, "metric": w.metric}
+            for label, thr in (("stream", 1 << 40), ("tile", 0)):
+                rq.rvq_set_stream_max_frames(thr)
+                for _ in range(5):
+                    rq.rvq_encode(rvq.dims, rvq.tables, xs, w.Q, codes, scratch)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 50
+                a.record()
+                for _ in range(reps):
+                    rq.rvq_encode(rvq.dims, rvq.tables, xs, w.Q, codes, scratch)
+                b.record()
+                torch.cuda.synchronize()
+                row[f"{label}_us"] = round(a.elapsed_time(b) / reps * 1e3, 2)
+                wall = []
+                for _ in range(30):
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                    rq.rvq_encode(rvq.dims, rvq.tables, xs, w.Q, codes, scratch)
+                    torch.cuda.synchronize()
+                    wall.append((time.perf_counter() - t0) * 1e6)
+                row[f"{label}_wall_us"] = round(float(np.median(wall)), 1)
+            rq.rvq_set_stream_max_frames(default)
+            row["speedup"] = round(row["tile_us"] / row["stream_us"], 2)
+            print(json.dumps(row), flush=True)
+        del rvq
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,12 +527,15 @@ def main():
     ap.add_argument("--frames", type=int, default=0, help="use only the first N frames (profiling)")
     ap.add_argument("--peaks", action="store_true", help="measure TF32/FP32 GEMM and L2 bandwidths instead")
     ap.add_argument("--table", action="store_true", help="per-workload encode/decode throughput instead")
+    ap.add_argument("--latency", action="store_true", help="small-batch encode latency per workload instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
     if args.peaks:
         measure_peaks()
     elif args.table:
         per_workload_table(args)
+    elif args.latency:
+        latency_table(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -261,7 +261,7 @@ RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const fl
  * d = 8, or d = 64 with K <= 4096 (and n_q <= 42 when K = 128); other shapes
  * use the tile kernels.  Sets the process-wide threshold (0 turns the small-batch kernel
  * off) and returns the previous one; a negative argument only returns the
- * current value.  The default is 64 frames.  Thread-safe; a change applies to
+ * current value.  The default is 512 frames.  Thread-safe; a change applies to
  * calls made after it. */
 RVQ_API int64_t rvq_set_stream_max_frames(int64_t max_frames);
 

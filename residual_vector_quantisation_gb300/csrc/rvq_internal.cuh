@@ -89,7 +89,7 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
 // codewords of every stage.  stream_supported: true if it takes a call of
 // n_frames frames at depth n_q (else the tile path does).
 constexpr int kStreamFrames = 16;
-constexpr int kStreamMaxFramesDefault = 64;
+constexpr int kStreamMaxFramesDefault = 512;
 __host__ __device__ inline int stream_cluster_size(int K) { return K / 128 < 8 ? K / 128 : 8; }
 bool stream_supported(const rvq_dims &dm, int n_q, int64_t n_frames);
 // p0: scratch for the stage projections ([n][n_q*d] f32); zero_status: the

@@ -164,7 +164,7 @@ constexpr int ST_BATCH = 8;                 // table rows in flight per thread i
 // Dynamic shared memory layout (byte offsets), the same on host and device.
 struct StreamShape {
   int CS, kc, NB, slots, n_own;
-  uint32_t pown, pin, cbuf, cnb, red, xch, loc, sv, bars, total;
+  uint32_t pown, pin, cbuf, cnb, red, xch, loc, csm, sv, bars, total;
 };
 
 __host__ __device__ inline uint32_t up16(uint32_t v) { return (v + 15u) & ~15u; }
@@ -186,13 +186,15 @@ __host__ __device__ inline StreamShape stream_shape(int d, int K, int n_q, int N
   S.red = o;  o = up16(o + (uint32_t)ST_F * S.slots * 8);                // [F][slots] keys
   S.xch = o;  o = up16(o + 2u * ST_MAX_CS * ST_F * 8);                  // [2][rank][F] exchanged keys
   S.loc = o;  o = up16(o + ST_F * 8);                                    // [F] this CTA's best keys
+  S.csm = o;  o = up16(o + 2u * ST_F * 4);                               // [2][F] codes of the last two stages
   S.sv = o;   o = up16(o + ST_F * 4);                                    // [F] distance scale s
-  S.bars = o; o = up16(o + 6u * 8);                                      // cb_full[2] x_full[2] p_full[2]
+  S.bars = o; o = up16(o + 7u * 8);                                      // cb_full[3] x_full[2] p_full[2]
   S.total = o;
   return S;
 }
 
-// Buffers for the codebook slices: 2 when two fit, else 1 (0: the shape does not fit).
+// Buffers for the codebook slices: 2 when two fit, else 1 (0: the shape does
+// not fit).  (A third buffer measured no faster: the copies land in time.)
 int stream_nb(int d, int K, int n_q) {
   if (stream_shape(d, K, n_q, 2).total <= ST_SMEM_LIMIT) return 2;
   if (stream_shape(d, K, n_q, 1).total <= ST_SMEM_LIMIT) return 1;
@@ -218,10 +220,6 @@ __device__ __forceinline__ void sub4(float4 &p, const float4 g) {
   p.w -= g.w;
 }
 
-__device__ __forceinline__ uint4 as_u4(const float4 v) {
-  return make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
-}
-
 // P0 [n][n_q*d] (k_project_small), codes [n][n_q].  grid: CS * ceil(n/16)
 // CTAs in clusters of CS; ST_THREADS threads.  SPLITJ: threads per codeword
 // (2 when kc == 128, each taking every other float4 column); NF: frames per
@@ -242,7 +240,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const int t = threadIdx.x;
   const int CS = S.CS, kc = S.kc;
   if (cluster_nctarank() != (uint32_t)CS || blockDim.x != ST_THREADS || dynamic_smem_size() < S.total ||
-      (SPLITJ == 2) != (kc == 128) || (NB != 1 && NB != 2) || (NF < ST_F && n > NF)) {
+      (SPLITJ == 2) != (kc == 128) || (NB != 1 && NB != 2 && NB != 3) || (NF < ST_F && n > NF)) {
     griddep_wait();  // after the projection kernel, which may clear the status word
     if (t == 0) st_error(status, RVQ_DEVICE_BAD_LAUNCH);
     return;  // uniform over the cluster: no CTA reaches a cluster barrier
@@ -259,9 +257,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   uint64_t *red = reinterpret_cast<uint64_t *>(smem + S.red); // [F][slots]
   uint64_t *xch = reinterpret_cast<uint64_t *>(smem + S.xch); // [2][ST_MAX_CS][F]
   uint64_t *loc = reinterpret_cast<uint64_t *>(smem + S.loc); // [F]
+  int *csm = reinterpret_cast<int *>(smem + S.csm);           // [2][F]
   float *sv = reinterpret_cast<float *>(smem + S.sv);         // [F]
   uint64_t *cb_full = reinterpret_cast<uint64_t *>(smem + S.bars);
-  uint64_t *x_full = cb_full + 2, *p_full = cb_full + 4;
+  uint64_t *x_full = cb_full + 3, *p_full = cb_full + 5;
 
   const uint32_t slice_bytes = (uint32_t)kc * d * 4, norm_bytes = (uint32_t)kc * 4;
   // transaction bytes of one exchange (keys from the other CS-1 CTAs) and of
@@ -273,18 +272,23 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     bulk_g2s(cbuf + (size_t)b * TPF * kc, cb_s + ((int64_t)q * CS + rank) * TPF * kc, slice_bytes, &cb_full[b]);
     bulk_g2s(cnb + (size_t)b * kc, cnorm + (int64_t)q * K + (int64_t)rank * kc, norm_bytes, &cb_full[b]);
   };
-  // push one float4 of stage q's projection (frame f, column j4) into every
-  // CTA (this one by a plain store: the same thread reads it back)
-  auto push = [&](int q, int f, int j4, const float4 v) {
-    float4 *slot = Pin + ((q & 1) * ST_F + f) * TPF + j4;
-    const uint32_t dst = smem_addr(slot), bar = smem_addr(&p_full[q & 1]);
-    for (int r = 0; r < CS; ++r)
-      if (r != (int)rank) st_async_u4(cluster_map(dst, (uint32_t)r), as_u4(v), cluster_map(bar, (uint32_t)r));
-    *slot = v;
+  // Push owned stage q's projection (rows 0 .. NF-1, every term but its
+  // last) into the other CTAs: lane 0 of warp r bulk-copies it to rank r (one
+  // copy per warp, so that no warp is held up issuing several).  The rows were
+  // written by generic stores, each writer fenced them for the async proxy,
+  // and a CTA barrier came in between.  This CTA's own copy is a plain store
+  // by the thread that owns the element.
+  auto push_remote = [&](int q) {
+    const int r = t >> 5;
+    if ((t & 31) == 0 && r < CS && r != (int)rank) {
+      const uint32_t dst = cluster_map(smem_addr(Pin + (q & 1) * ST_F * TPF), (uint32_t)r);
+      const uint32_t bar = cluster_map(smem_addr(&p_full[q & 1]), (uint32_t)r);
+      bulk_s2cluster(dst, Pown + (q / CS) * ST_F * TPF, (uint32_t)NF * TPF * 16, bar);
+    }
   };
 
   if (t == 0) {
-    for (int b = 0; b < NB; ++b) mbar_init(&cb_full[b], 1);
+    for (int b = 0; b < NB; ++b) mbar_init(&cb_full[b], 1);  // NB <= 3 (the layout holds 6 barriers + 3)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&x_full[b], 1);
       mbar_init(&p_full[b], 1);
@@ -311,12 +315,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     if (q < n_q && f < nf) v = __ldg(reinterpret_cast<const float4 *>(P0 + (f0 + f) * n_cols + q * d) + j4);
     Pown[(i * ST_F + f) * TPF + j4] = v;
   }
+  fence_proxy_async_smem();
   __syncthreads();
   cluster_wait();
   for (int q = 0; q < 2 && q < n_q; ++q)  // stages 0 and 1 need no cross-stage term before the push
-    if (q % CS == (int)rank && t < NF * TPF) {
-      const int f = t / TPF, j4 = t % TPF;
-      push(q, f, j4, Pown[((q / CS) * ST_F + f) * TPF + j4]);
+    if (q % CS == (int)rank) {
+      push_remote(q);
+      if (t < NF * TPF) Pin[(q & 1) * ST_F * TPF + t] = Pown[(q / CS) * ST_F * TPF + t];
     }
   if (!mbar_wait_cluster_hot(&p_full[0], 0)) st_error(status, RVQ_DEVICE_TIMEOUT);
   __syncthreads();  // this CTA's own pushes are visible
@@ -333,17 +338,20 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   // ---- the stage loop -------------------------------------------------------
   const int h = SPLITJ == 2 ? (t & 1) : 0;
   const int kk0 = SPLITJ == 2 ? (t >> 1) : t;
+  int b = 0;         // slice buffer of stage q (q mod NB)
+  uint32_t ph = 0;   // its phase parity ((q / NB) & 1)
   for (int q = 0; q < n_q; ++q) {
-    const int b = NB == 2 ? (q & 1) : 0;
     // Re-arm the barriers whose last phase every thread has now seen (stage
     // q's push, stage q-1's exchange).  Not earlier: an arm that expects no
     // bytes completes the next phase at once, and a thread still waiting on
-    // the previous phase would then miss it.
-    if (t == 0) {
+    // the previous phase would then miss it.  The last thread does it: it
+    // stores no codes, so its arrive (a release) waits for no global store.
+    if (t == ST_THREADS - 1) {
       if (q + 2 < n_q) mbar_arrive_expect_tx(&p_full[q & 1], p_bytes(q + 2));
       if (q >= 1 && q + 1 < n_q) mbar_arrive_expect_tx(&x_full[(q + 1) & 1], x_bytes);
     }
-    if (!mbar_wait(&cb_full[b], (uint32_t)((NB == 2 ? q >> 1 : q) & 1))) st_error(status, RVQ_DEVICE_TIMEOUT);
+    if (q >= 1 && q + 1 < n_q && (q + 1) % CS == (int)rank) push_remote(q + 1);  // updated at the end of stage q-1
+    if (!mbar_wait_hot(&cb_full[b], ph)) st_error(status, RVQ_DEVICE_TIMEOUT);
 
     // distances of this CTA's slice; per frame the smallest key
     uint64_t best[NF];
@@ -405,12 +413,40 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
       fence_proxy_async_smem();
       issue(q + NB, b);
     }
-    if (t < CS && t != (int)rank) {  // this CTA's keys to rank t (its own stay in loc)
-      const uint32_t dst = cluster_map(smem_addr(xch + ((q & 1) * ST_MAX_CS + rank) * ST_F), (uint32_t)t);
-      const uint32_t bar = cluster_map(smem_addr(&x_full[q & 1]), (uint32_t)t);
-      const uint4 *l4 = reinterpret_cast<const uint4 *>(loc);
+    if (t < (CS - 1) * NU) {  // this CTA's keys to the other ranks, 16 bytes a thread (its own stay in loc)
+      const int di = t / NU, u = t % NU, r = di < (int)rank ? di : di + 1;
+      const uint32_t dst = cluster_map(smem_addr(xch + ((q & 1) * ST_MAX_CS + rank) * ST_F), (uint32_t)r);
+      const uint32_t bar = cluster_map(smem_addr(&x_full[q & 1]), (uint32_t)r);
+      st_async_u4(dst + 16u * u, reinterpret_cast<const uint4 *>(loc)[u], bar);
+    }
+
+    // while the keys travel: the previous code's terms for this CTA's stages
+    // q' >= q+2 (q' = rank mod CS); stage q+2's first element goes to the
+    // thread that applies its next term at the end of this stage
+    if (q >= 1) {
+      const int *cprev = csm + ((q - 1) & 1) * ST_F;
+      const int first = (q + 2 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
+      const int items = S.n_own > first ? (S.n_own - first) * NF * TPF : 0;
+      for (int e0 = t; e0 < items; e0 += ST_THREADS * ST_BATCH) {
+        float4 gv[ST_BATCH];
 #pragma unroll
-      for (int i = 0; i < NU; ++i) st_async_u4(dst + 16u * i, l4[i], bar);
+        for (int u = 0; u < ST_BATCH; ++u) {
+          const int e = e0 + u * ST_THREADS;
+          if (e < items) {
+            const int i = first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
+            const int qq = (int)rank + i * CS;
+            if (qq < n_q) gv[u] = __ldg(g + (pair_index(qq, q - 1) * K + cprev[f]) * TPF + j4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < ST_BATCH; ++u) {
+          const int e = e0 + u * ST_THREADS;
+          if (e < items) {
+            const int i = first + e / (NF * TPF), fj = e % (NF * TPF);
+            if ((int)rank + i * CS < n_q) sub4(Pown[i * ST_F * TPF + fj], gv[u]);
+          }
+        }
+      }
     }
 
     // the exchange: the code of every frame
@@ -430,7 +466,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     if (t < NF * TPF) {
       const int f = t / TPF, j4 = t % TPF;
       const uint32_t code = code_of(f);
-      if (rank == 0 && j4 == 0 && f < nf) codes[(f0 + f) * n_q + q] = (int32_t)code;
+      if (j4 == 0) {
+        csm[(q & 1) * ST_F + f] = (int)code;
+        if (rank == 0 && f < nf) codes[(f0 + f) * n_q + q] = (int32_t)code;
+      }
       float4 g1, g2;
       if (q + 1 < n_q) g1 = __ldg(g + (pair_index(q + 1, q) * K + code) * TPF + j4);
       if (own2) g2 = __ldg(g + (pair_index(q + 2, q) * K + code) * TPF + j4);
@@ -444,38 +483,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
           if (j4 == 0) sv[f] = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
         }
       }
-      if (own2) {  // stage q+2 has every term but its last: push it
+      if (own2) {  // stage q+2 has every term but its last: pushed at the top of the next stage
         float4 &pv = Pown[(((q + 2) / CS) * ST_F + f) * TPF + j4];
         sub4(pv, g2);
-        push(q + 2, f, j4, pv);
-      }
-    }
-    {  // this CTA's later stages q' >= q+3 (q' = rank mod CS)
-      const int first = (q + 3 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
-      const int n_later = S.n_own - first;
-      const int items = n_later > 0 ? n_later * NF * TPF : 0;
-      for (int e0 = t; e0 < items; e0 += ST_THREADS * ST_BATCH) {
-        float4 gv[ST_BATCH];
-#pragma unroll
-        for (int u = 0; u < ST_BATCH; ++u) {
-          const int e = e0 + u * ST_THREADS;
-          if (e < items) {
-            const int i = first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
-            const int qq = (int)rank + i * CS;
-            if (qq < n_q) gv[u] = __ldg(g + (pair_index(qq, q) * K + code_of(f)) * TPF + j4);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < ST_BATCH; ++u) {
-          const int e = e0 + u * ST_THREADS;
-          if (e < items) {
-            const int i = first + e / (NF * TPF), fj = e % (NF * TPF);
-            if ((int)rank + i * CS < n_q) sub4(Pown[i * ST_F * TPF + fj], gv[u]);
-          }
-        }
+        Pin[(((q + 2) & 1) * ST_F + f) * TPF + j4] = pv;
+        fence_proxy_async_smem();
       }
     }
     __syncthreads();
+    if (++b == NB) {
+      b = 0;
+      ph ^= 1u;
+    }
   }
 
   // a slice copy whose wait gave up may still be landing: wait (bounded) for it
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     for (int b = 0; b < NB; ++b) {
       int last = -1;
       for (int q = b; q < n_q; q += NB) last = q;
-      if (last >= 0) mbar_wait(&cb_full[b], (uint32_t)((NB == 2 ? last >> 1 : last) & 1));
+      if (last >= 0) mbar_wait(&cb_full[b], (uint32_t)((last / NB) & 1));
     }
   }
   cluster_sync_all();  // no CTA leaves while another may still address its shared memory

@@ -298,6 +298,15 @@ __device__ __forceinline__ void st_async_u4(uint32_t addr, uint4 v, uint32_t bar
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
                : "memory");
 }
+// Bulk copy from this CTA's shared memory into the shared memory of a CTA of
+// the cluster; the bytes count toward the transaction count of the mbarrier
+// `bar` in that CTA (`dst` and `bar` are cluster-window addresses).  Both
+// addresses and the size are multiples of 16.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void *src_smem, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_addr(src_smem)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue now / wait until the previous kernel has finished and its writes
 // are visible.
