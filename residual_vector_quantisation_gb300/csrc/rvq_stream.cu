@@ -1,8 +1,8 @@
 // Low-latency RVQ encode of small batches: the streaming path.
 //
-// Realtime callers encode a few frames at a time: omnivoice.cpp
-// ARCHITECTURE.md ("CLI tools", omnivoice-tts) starts synthesis from stdin as
-// soon as the first sentence is complete, and moss-tts.cpp AGENTS.md has a
+// Realtime callers encode a few frames at a time: the omnivoice-tts tool of
+// omnivoice.cpp ARCHITECTURE.md ("CLI tools") begins synthesising once a first
+// sentence of its streamed text is complete, and moss-tts.cpp AGENTS.md has a
 // realtime TTS front end.  For such calls the tile path (128-frame tiles, one
 // CTA per tile walking all K codewords of every stage) leaves the GPU idle
 // and its latency is the serial walk over Q*K codewords.  Here:
