@@ -462,7 +462,8 @@ def latency_table(args):
     rvq_set_stream_max_frames frames) and, for comparison, on the tile kernels
     (threshold 0).  Per call: CUDA-event time of back-to-back calls on one
     stream, and the median host wall time of a single call with a synchronize
-    (launch overhead included)."""
+    (launch overhead included); for the streaming kernels also the wall time
+    of one replay of the call captured in a CUDA graph."""
     import torch
     import residual_vector_quantisation_gb300 as rq
     dev = torch.device("cuda", 0)
@@ -505,6 +506,21 @@ def latency_table(args):
                     torch.cuda.synchronize()
                     wall.append((time.perf_counter() - t0) * 1e6)
                 row[f"{label}_wall_us"] = round(float(np.median(wall)), 1)
+                if label == "stream":  # the same call replayed from a captured CUDA graph
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+                        rq.rvq_encode(rvq.dims, rvq.tables, xs, w.Q, codes, scratch)
+                    for _ in range(5):
+                        graph.replay()
+                    wall = []
+                    for _ in range(30):
+                        torch.cuda.synchronize()
+                        t0 = time.perf_counter()
+                        graph.replay()
+                        torch.cuda.synchronize()
+                        wall.append((time.perf_counter() - t0) * 1e6)
+                    row["stream_graph_wall_us"] = round(float(np.median(wall)), 1)
+                    del graph
             rq.rvq_set_stream_max_frames(default)
             row["speedup"] = round(row["tile_us"] / row["stream_us"], 2)
             print(json.dumps(row), flush=True)
@@ -522,7 +538,7 @@ def main():
     ap.add_argument("--ref-frames", type=int, default=8192, help="oracle frames per step for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-chunk", type=int, default=19456, help="frames per chunk of the host pipeline")
+    ap.add_argument("--e2e-chunk", type=int, default=9728, help="frames per chunk of the host pipeline")
     ap.add_argument("--workload", default=WORKLOAD, choices=[w.name for w in ri.WORKLOADS])
     ap.add_argument("--frames", type=int, default=0, help="use only the first N frames (profiling)")
     ap.add_argument("--peaks", action="store_true", help="measure TF32/FP32 GEMM and L2 bandwidths instead")

@@ -34,7 +34,11 @@ def test_pipeline_matches_device_path(rvq, n, chunk, n_q):
     x_host = x.pin_memory()
     pipe = rq.RVQPipeline(rvq, n_q=n_q, chunk_frames=chunk)
     codes_h, x_hat_h = pipe.reconstruct(x_host)
-    codes_d, x_hat_d = rvq.reconstruct(x.to(DEV), n_q=n_q)
+    # the device path on the same chunks (a chunk of up to rvq_set_stream_max_frames
+    # frames runs on the small-batch kernels, a larger one on the tile kernels)
+    parts = [rvq.reconstruct(x[c0:c0 + chunk].to(DEV), n_q=n_q) for c0 in range(0, n, chunk)]
+    codes_d = torch.cat([c for c, _ in parts])
+    x_hat_d = torch.cat([y for _, y in parts])
     torch.cuda.synchronize()
     assert torch.equal(codes_h, codes_d.cpu())
     assert torch.equal(x_hat_h, x_hat_d.cpu())
@@ -42,6 +46,24 @@ def test_pipeline_matches_device_path(rvq, n, chunk, n_q):
     codes2, none = pipe.reconstruct(x_host, want_x_hat=False)
     assert none is None and torch.equal(codes2, codes_h)
     pipe.close()
+
+
+@pytest.mark.parametrize("threshold", [0, 1 << 40])
+def test_pipeline_on_each_encode_path(rvq, threshold):
+    """Chunks of 300 frames on the tile kernels (threshold 0) and on the
+    small-batch kernels: the same codes as the device path on those chunks."""
+    prev = rq.rvq_set_stream_max_frames(threshold)
+    try:
+        n, chunk = 900, 300
+        x = torch.from_numpy(np.random.default_rng(7).standard_normal((n, rvq.D)).astype(np.float32))
+        pipe = rq.RVQPipeline(rvq, chunk_frames=chunk)
+        codes_h, _ = pipe.reconstruct(x.pin_memory(), want_x_hat=False)
+        codes_d = torch.cat([rvq.encode(x[c0:c0 + chunk].to(DEV)) for c0 in range(0, n, chunk)])
+        torch.cuda.synchronize()
+        assert torch.equal(codes_h, codes_d.cpu())
+        pipe.close()
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
 
 
 def test_pipeline_rejects_bad_arguments(rvq):

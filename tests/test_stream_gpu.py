@@ -258,3 +258,32 @@ def test_the_streaming_kernel_runs():
     kt = kernels(0)
     assert not any("k_encode_stream" in k for k in kt), kt
     assert any("k_search" in k for k in kt), kt
+
+
+@pytest.mark.parametrize("threshold", [ALL, 0])
+def test_encode_replayed_from_a_cuda_graph(threshold):
+    """The realtime pattern: one encode of a 16-frame buffer captured into a CUDA
+    graph, then replayed for each new group of frames copied into that buffer.
+    Every replay gives the eager call's codes (small-batch kernels with a
+    programmatic dependent launch, or the tile kernels with threshold 0)."""
+    w = ri.WORKLOAD_BY_NAME["omnivoice"]
+    W = ri.make_weights(w)
+    frames = torch.from_numpy(ri.make_x(w, W)[:48]).to(DEV)
+    rvq = make_rvq(W)
+    x = frames[:16].clone()
+    codes = torch.empty((16, w.Q), dtype=torch.int32, device=DEV)
+    with stream_max(threshold):
+        scratch = rvq.scratch_for(16, w.Q)
+        rq.rvq_encode(rvq.dims, rvq.tables, x, w.Q, codes, scratch)  # first call: kernel attributes set
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+            rq.rvq_encode(rvq.dims, rvq.tables, x, w.Q, codes, scratch)
+        for g0 in (0, 16, 32):
+            x.copy_(frames[g0:g0 + 16])
+            codes.fill_(-1)
+            graph.replay()
+            eager = rvq.encode(frames[g0:g0 + 16].clone())
+            torch.cuda.synchronize()
+            assert torch.equal(codes, eager), f"replay of frames {g0}.."
+            assert device_status(rvq) == 0
