@@ -223,8 +223,10 @@ __device__ __forceinline__ void sub4(float4 &p, const float4 g) {
 // P0 [n][n_q*d] (k_project_small), codes [n][n_q].  grid: CS * ceil(n/16)
 // CTAs in clusters of CS; ST_THREADS threads.  SPLITJ: threads per codeword
 // (2 when kc == 128, each taking every other float4 column); NF: frames per
-// cluster computed (16, or fewer when the whole call has fewer).
-template <int d, int SPLITJ, int NF>
+// cluster computed (16, or fewer when the whole call has fewer); CW:
+// codewords a thread scores together (2 when kc == 512, sharing the loads of
+// the frames' projections).
+template <int d, int SPLITJ, int NF, int CW>
 __global__ void __launch_bounds__(ST_THREADS, 1)
     k_stream_search(const float *__restrict__ P0, const float4 *__restrict__ cb_s, const float *__restrict__ cnorm,
                     const float4 *__restrict__ g, int32_t *__restrict__ codes, int64_t n, int K, int n_q, int NB,
@@ -240,7 +242,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const int t = threadIdx.x;
   const int CS = S.CS, kc = S.kc;
   if (cluster_nctarank() != (uint32_t)CS || blockDim.x != ST_THREADS || dynamic_smem_size() < S.total ||
-      (SPLITJ == 2) != (kc == 128) || (NB != 1 && NB != 2 && NB != 3) || (NF < ST_F && n > NF)) {
+      (SPLITJ == 2) != (kc == 128) || kc % (CW * (ST_THREADS / SPLITJ)) != 0 || (NB != 1 && NB != 2 && NB != 3) ||
+      (NF < ST_F && n > NF)) {
     griddep_wait();  // after the projection kernel, which may clear the status word
     if (t == 0) st_error(status, RVQ_DEVICE_BAD_LAUNCH);
     return;  // uniform over the cluster: no CTA reaches a cluster barrier
@@ -361,37 +364,49 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
       const float4 *cq = cbuf + (size_t)b * TPF * kc;
       const float *cnq = cnb + (size_t)b * kc;
       const float4 *pq = Pin + (q & 1) * ST_F * TPF;
-      for (int kk = kk0; kk < kc; kk += ST_THREADS / SPLITJ) {
-        // dot products of the codeword with every frame, its columns taken
-        // CH float4 at a time (in column order) to bound the registers
+      constexpr int KSTEP = ST_THREADS / SPLITJ;  // codewords scored by the CTA per pass
+      for (int kk = kk0; kk < kc; kk += CW * KSTEP) {
+        // dot products of the thread's CW codewords with every frame, the
+        // columns taken CH float4 at a time (in column order) to bound the
+        // registers; each frame's projection is loaded once for all CW
         constexpr int CH = DJ4 < 8 ? DJ4 : 8;
-        float a[NF];
+        float a[CW][NF];
 #pragma unroll
-        for (int f = 0; f < NF; ++f) a[f] = 0.0f;
+        for (int w = 0; w < CW; ++w)
+#pragma unroll
+          for (int f = 0; f < NF; ++f) a[w][f] = 0.0f;
 #pragma unroll 1
         for (int m0 = 0; m0 < DJ4; m0 += CH) {
-          float4 c[CH];
+          float4 c[CW][CH];
 #pragma unroll
-          for (int m = 0; m < CH; ++m) c[m] = cq[((m0 + m) * SPLITJ + h) * kc + kk];
+          for (int w = 0; w < CW; ++w)
+#pragma unroll
+            for (int m = 0; m < CH; ++m) c[w][m] = cq[((m0 + m) * SPLITJ + h) * kc + kk + w * KSTEP];
 #pragma unroll
           for (int f = 0; f < NF; ++f) {
             const float4 *pf = pq + f * TPF + h;
 #pragma unroll
             for (int m = 0; m < CH; ++m) {
               const float4 pv = pf[(m0 + m) * SPLITJ];
-              a[f] = fmaf(c[m].x, pv.x, a[f]);
-              a[f] = fmaf(c[m].y, pv.y, a[f]);
-              a[f] = fmaf(c[m].z, pv.z, a[f]);
-              a[f] = fmaf(c[m].w, pv.w, a[f]);
+#pragma unroll
+              for (int w = 0; w < CW; ++w) {
+                a[w][f] = fmaf(c[w][m].x, pv.x, a[w][f]);
+                a[w][f] = fmaf(c[w][m].y, pv.y, a[w][f]);
+                a[w][f] = fmaf(c[w][m].z, pv.z, a[w][f]);
+                a[w][f] = fmaf(c[w][m].w, pv.w, a[w][f]);
+              }
             }
           }
         }
-        const float cn = cnq[kk];
-        const uint32_t kg = rank * (uint32_t)kc + (uint32_t)kk;
 #pragma unroll
-        for (int f = 0; f < NF; ++f) {
-          if (SPLITJ == 2) a[f] += __shfl_xor_sync(0xffffffffu, a[f], 1);
-          best[f] = min_u64(best[f], dist_key(fmaf(-2.0f * sv[f], a[f], cn), kg));
+        for (int w = 0; w < CW; ++w) {
+          const float cn = cnq[kk + w * KSTEP];
+          const uint32_t kg = rank * (uint32_t)kc + (uint32_t)(kk + w * KSTEP);
+#pragma unroll
+          for (int f = 0; f < NF; ++f) {
+            if (SPLITJ == 2) a[w][f] += __shfl_xor_sync(0xffffffffu, a[w][f], 1);
+            best[f] = min_u64(best[f], dist_key(fmaf(-2.0f * sv[f], a[w][f], cn), kg));
+          }
         }
       }
     }
@@ -511,18 +526,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
 std::atomic<unsigned long long> g_stream_attr_done{0};
 std::atomic<int64_t> g_stream_max_frames{kStreamMaxFramesDefault};
 
-template <int d, int SPLITJ>
+template <int d, int SPLITJ, int CW>
 cudaError_t set_search_attrs() {
   cudaError_t e = cudaSuccess;
   auto set = [&](auto kern) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ST_SMEM_LIMIT);
   };
-  set(k_stream_search<d, SPLITJ, 1>);
-  set(k_stream_search<d, SPLITJ, 2>);
-  set(k_stream_search<d, SPLITJ, 4>);
-  set(k_stream_search<d, SPLITJ, 8>);
-  set(k_stream_search<d, SPLITJ, 16>);
+  set(k_stream_search<d, SPLITJ, 1, CW>);
+  set(k_stream_search<d, SPLITJ, 2, CW>);
+  set(k_stream_search<d, SPLITJ, 4, CW>);
+  set(k_stream_search<d, SPLITJ, 8, CW>);
+  set(k_stream_search<d, SPLITJ, 16, CW>);
   return e;
 }
 
@@ -535,33 +550,34 @@ cudaError_t ensure_stream_attributes() {
   if ((e = cudaFuncSetAttribute(k_project_small, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_SMEM)) !=
       cudaSuccess)
     return e;
-  if ((e = set_search_attrs<kCodeDim, 2>()) != cudaSuccess) return e;
-  if ((e = set_search_attrs<kCodeDim, 1>()) != cudaSuccess) return e;
-  if ((e = set_search_attrs<kCodeDimSmall, 2>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDim, 2, 1>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDim, 1, 1>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDim, 1, 2>()) != cudaSuccess) return e;
+  if ((e = set_search_attrs<kCodeDimSmall, 2, 1>()) != cudaSuccess) return e;
   g_stream_attr_done.fetch_or(bit);
   return cudaSuccess;
 }
 
-template <int d, int SPLITJ>
+template <int d, int SPLITJ, int CW>
 cudaError_t launch_search(cudaLaunchConfig_t &cfg, int nf_max, const float *p0, const float4 *cb_s, const float *cn,
                           const float4 *g, int32_t *codes, int64_t n, int K, int n_q, int NB, int metric,
                           int *status) {
   switch (nf_max) {
     case 1:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 1>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
-                                status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 1, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                                metric, status);
     case 2:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 2>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
-                                status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 2, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                                metric, status);
     case 4:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 4>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
-                                status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 4, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                                metric, status);
     case 8:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 8>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
-                                status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 8, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                                metric, status);
     default:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16>, p0, cb_s, cn, g, codes, n, K, n_q, NB, metric,
-                                status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                                metric, status);
   }
 }
 
@@ -609,10 +625,13 @@ cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const f
   const float4 *cb_s = at<float4>(tables, L.cb_stream), *g = at<float4>(tables, L.g);
   const float *cn = at<float>(tables, L.cnorm);
   if (dm.d == kCodeDimSmall)
-    return launch_search<kCodeDimSmall, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+    return launch_search<kCodeDimSmall, 2, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric,
+                                              status);
   if (S.kc == 128)
-    return launch_search<kCodeDim, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
-  return launch_search<kCodeDim, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+    return launch_search<kCodeDim, 2, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+  if (S.kc == 256)
+    return launch_search<kCodeDim, 1, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+  return launch_search<kCodeDim, 1, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
 }
 
 }  // namespace rvq
