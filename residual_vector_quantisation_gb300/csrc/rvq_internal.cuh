@@ -29,6 +29,11 @@ __host__ __device__ inline int64_t pair_index(int q, int s) { return (int64_t)q 
 inline int dim_in(const rvq_dims &dm) { return dm.D_in > 0 ? dm.D_in : dm.D; }
 inline int dim_out(const rvq_dims &dm) { return dm.D_out > 0 ? dm.D_out : dm.D; }
 
+// Whether the shape can take the small-batch (streaming) kernels at all, i.e.
+// whether the tables include their copies (w_in_f, cb_stream): d = 8, or
+// d = 64 with slices of at most 512 codewords (K <= 4096).
+inline bool stream_tables(const rvq_dims &dm) { return dm.d != kCodeDim || dm.K <= 4096; }
+
 // Byte offsets of the prepared tables inside the caller's tables buffer.
 struct TablesLayout {
   size_t w_in_hi;  // [Q*d][D_in]  f32, TF32-truncated high part of w_in (. fc_w)
@@ -67,8 +72,9 @@ inline TablesLayout tables_layout(const rvq_dims &dm) {
   L.m64 = take((P ? P : 1) * d * d * 8);
   L.vb64 = take((P ? P : 1) * d * 8);
   L.m2_64 = take(Q * Do * (d + 1) * 8);
-  L.w_in_f = take(Q * d * Di * 4);
-  L.cb_stream = take(Q * K * d * 4);
+  const bool st = stream_tables(dm);  // the streaming copies, else empty
+  L.w_in_f = take(st ? Q * d * Di * 4 : 0);
+  L.cb_stream = take(st ? Q * K * d * 4 : 0);
   L.total = o;
   return L;
 }

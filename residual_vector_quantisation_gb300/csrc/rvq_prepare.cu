@@ -321,7 +321,7 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
     k_prep_w_in<<<608, 256, 0, st>>>(w.w_in, w.b_in, at<float>(tables, L.w_in_hi), at<float>(tables, L.w_in_lo),
                                      at<float>(tables, L.b_in), nw, (int64_t)Q * d);
   }
-  {  // the streaming path's copies: w_in' in float32, the sliced (normalised) codebook
+  if (stream_tables(dm)) {  // the streaming path's copies: w_in' in float32, the sliced (normalised) codebook
     const int D_in = dim_in(dm);
     const int64_t nt = (int64_t)Q * D_in * d, nc = (int64_t)Q * K * d;
     k_prep_w_in_f<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(at<float>(tables, L.w_in_hi),

@@ -586,11 +586,8 @@ cudaError_t launch_search(cudaLaunchConfig_t &cfg, int nf_max, const float *p0, 
 bool stream_supported(const rvq_dims &dm, int n_q, int64_t n_frames) {
   if (n_frames < 1 || n_frames > g_stream_max_frames.load()) return false;
   if (dm.K % 128 != 0 || dm.K < 128) return false;
-  if (dm.d == kCodeDim) {
-    if (dm.K > 4096) return false;  // slices of at most 512 codewords
-  } else if (dm.d != kCodeDimSmall || dm.K > kMaxKSmall) {
-    return false;
-  }
+  if (!stream_tables(dm)) return false;  // d = 64 with K > 4096: slices of more than 512 codewords
+  if (dm.d != kCodeDim && (dm.d != kCodeDimSmall || dm.K > kMaxKSmall)) return false;
   return stream_nb(dm.d, dm.K, n_q) > 0;
 }
 
