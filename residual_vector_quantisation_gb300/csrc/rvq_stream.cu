@@ -354,6 +354,29 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
       if (q >= 1 && q + 1 < n_q) mbar_arrive_expect_tx(&x_full[(q + 1) & 1], x_bytes);
     }
     if (q >= 1 && q + 1 < n_q && (q + 1) % CS == (int)rank) push_remote(q + 1);  // updated at the end of stage q-1
+
+    // The previous code's terms for this CTA's stages q' >= q+2 (q' = rank mod
+    // CS), applied while this stage's keys travel.  The rows of the first PF
+    // items of each thread are loaded now, so that their latency passes during
+    // the distances; item e is (owned stage first + e / (NF*TPF), frame, column),
+    // so stage q+2's element (f, j4) goes to thread f*TPF + j4 -- the thread
+    // that applies its next term at the end of this stage.
+    constexpr int PF = SPLITJ == 2 ? 4 : (NF == 16 ? 1 : 2);
+    const int later_first = (q + 2 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
+    const int later_items = q >= 1 && S.n_own > later_first ? (S.n_own - later_first) * NF * TPF : 0;
+    const int *cprev = csm + ((q - 1) & 1) * ST_F;
+    auto later_row = [&](int e) -> const float4 * {  // nullptr past the last stage
+      const int i = later_first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
+      const int qq = (int)rank + i * CS;
+      return qq < n_q ? g + (pair_index(qq, q - 1) * K + cprev[f]) * TPF + j4 : nullptr;
+    };
+    float4 pre[PF];
+#pragma unroll
+    for (int u = 0; u < PF; ++u) {
+      const int e = t + u * ST_THREADS;
+      const float4 *row = e < later_items ? later_row(e) : nullptr;
+      if (row) pre[u] = __ldg(row);
+    }
     if (!mbar_wait_hot(&cb_full[b], ph)) st_error(status, RVQ_DEVICE_TIMEOUT);
 
     // distances of this CTA's slice; per frame the smallest key
@@ -435,31 +458,27 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
       st_async_u4(dst + 16u * u, reinterpret_cast<const uint4 *>(loc)[u], bar);
     }
 
-    // while the keys travel: the previous code's terms for this CTA's stages
-    // q' >= q+2 (q' = rank mod CS); stage q+2's first element goes to the
-    // thread that applies its next term at the end of this stage
-    if (q >= 1) {
-      const int *cprev = csm + ((q - 1) & 1) * ST_F;
-      const int first = (q + 2 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
-      const int items = S.n_own > first ? (S.n_own - first) * NF * TPF : 0;
-      for (int e0 = t; e0 < items; e0 += ST_THREADS * ST_BATCH) {
+    // while the keys travel: apply the deferred terms (the prefetched rows
+    // first, then any further items in batches)
+    if (later_items > 0) {
+#pragma unroll
+      for (int u = 0; u < PF; ++u) {
+        const int e = t + u * ST_THREADS;
+        if (e < later_items && later_row(e)) sub4(Pown[(later_first + e / (NF * TPF)) * ST_F * TPF + e % (NF * TPF)], pre[u]);
+      }
+      for (int e0 = t + PF * ST_THREADS; e0 < later_items; e0 += ST_THREADS * ST_BATCH) {
         float4 gv[ST_BATCH];
 #pragma unroll
         for (int u = 0; u < ST_BATCH; ++u) {
           const int e = e0 + u * ST_THREADS;
-          if (e < items) {
-            const int i = first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
-            const int qq = (int)rank + i * CS;
-            if (qq < n_q) gv[u] = __ldg(g + (pair_index(qq, q - 1) * K + cprev[f]) * TPF + j4);
-          }
+          const float4 *row = e < later_items ? later_row(e) : nullptr;
+          if (row) gv[u] = __ldg(row);
         }
 #pragma unroll
         for (int u = 0; u < ST_BATCH; ++u) {
           const int e = e0 + u * ST_THREADS;
-          if (e < items) {
-            const int i = first + e / (NF * TPF), fj = e % (NF * TPF);
-            if ((int)rank + i * CS < n_q) sub4(Pown[i * ST_F * TPF + fj], gv[u]);
-          }
+          if (e < later_items && later_row(e))
+            sub4(Pown[(later_first + e / (NF * TPF)) * ST_F * TPF + e % (NF * TPF)], gv[u]);
         }
       }
     }
