@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   };
 
   if (t == 0) {
-    for (int b = 0; b < NB; ++b) mbar_init(&cb_full[b], 1);  // NB <= 3 (the layout holds 6 barriers + 3)
+    for (int b = 0; b < NB; ++b) mbar_init(&cb_full[b], 1);  // NB <= 3: the layout has three slice barriers
     for (int b = 0; b < 2; ++b) {
       mbar_init(&x_full[b], 1);
       mbar_init(&p_full[b], 1);
@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     const int i = e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
     const int q = (int)rank + i * CS;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q < n_q && f < nf) v = __ldg(reinterpret_cast<const float4 *>(P0 + (f0 + f) * n_cols + q * d) + j4);
+    // (through L2 only: P0 was written by the kernel this one overlapped)
+    if (q < n_q && f < nf) v = __ldcg(reinterpret_cast<const float4 *>(P0 + (f0 + f) * n_cols + q * d) + j4);
     Pown[(i * ST_F + f) * TPF + j4] = v;
   }
   fence_proxy_async_smem();
