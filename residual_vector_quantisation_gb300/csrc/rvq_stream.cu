@@ -224,8 +224,9 @@ __device__ __forceinline__ void sub4(float4 &p, const float4 g) {
 // CTAs in clusters of CS; ST_THREADS threads.  SPLITJ: threads per codeword
 // (2 when kc == 128, each taking every other float4 column); NF: frames per
 // cluster computed (16, or fewer when the whole call has fewer); CW:
-// codewords a thread scores together (2 when kc == 512, sharing the loads of
-// the frames' projections).
+// codewords a thread scores together (2 when kc is a multiple of 512, sharing
+// the loads of the frames' projections; otherwise a thread takes codewords
+// kk, kk + 256, ... one at a time, and kc need not be a multiple of 256).
 template <int d, int SPLITJ, int NF, int CW>
 __global__ void __launch_bounds__(ST_THREADS, 1)
     k_stream_search(const float *__restrict__ P0, const float4 *__restrict__ cb_s, const float *__restrict__ cnorm,
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const int t = threadIdx.x;
   const int CS = S.CS, kc = S.kc;
   if (cluster_nctarank() != (uint32_t)CS || blockDim.x != ST_THREADS || dynamic_smem_size() < S.total ||
-      (SPLITJ == 2) != (kc == 128) || kc % (CW * (ST_THREADS / SPLITJ)) != 0 || (NB != 1 && NB != 2 && NB != 3) ||
+      (SPLITJ == 2) != (kc == 128) || (CW == 2 && kc % (2 * ST_THREADS) != 0) || (NB != 1 && NB != 2 && NB != 3) ||
       (NF < ST_F && n > NF)) {
     griddep_wait();  // after the projection kernel, which may clear the status word
     if (t == 0) st_error(status, RVQ_DEVICE_BAD_LAUNCH);
@@ -366,10 +367,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     const int later_first = (q + 2 - (int)rank + CS - 1) / CS;  // owned index of the first such stage
     const int later_items = q >= 1 && S.n_own > later_first ? (S.n_own - later_first) * NF * TPF : 0;
     const int *cprev = csm + ((q - 1) & 1) * ST_F;
+    auto later_stage = [&](int e) { return (int)rank + (later_first + e / (NF * TPF)) * CS; };
     auto later_row = [&](int e) -> const float4 * {  // nullptr past the last stage
-      const int i = later_first + e / (NF * TPF), fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF;
-      const int qq = (int)rank + i * CS;
+      const int fj = e % (NF * TPF), f = fj / TPF, j4 = fj % TPF, qq = later_stage(e);
       return qq < n_q ? g + (pair_index(qq, q - 1) * K + cprev[f]) * TPF + j4 : nullptr;
+    };
+    auto later_part = [&](int e) -> float4 & {  // the owned stage's element of item e
+      return Pown[(later_first + e / (NF * TPF)) * ST_F * TPF + e % (NF * TPF)];
     };
     float4 pre[PF];
 #pragma unroll
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
 #pragma unroll
       for (int u = 0; u < PF; ++u) {
         const int e = t + u * ST_THREADS;
-        if (e < later_items && later_row(e)) sub4(Pown[(later_first + e / (NF * TPF)) * ST_F * TPF + e % (NF * TPF)], pre[u]);
+        if (e < later_items && later_stage(e) < n_q) sub4(later_part(e), pre[u]);
       }
       for (int e0 = t + PF * ST_THREADS; e0 < later_items; e0 += ST_THREADS * ST_BATCH) {
         float4 gv[ST_BATCH];
@@ -478,8 +482,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
 #pragma unroll
         for (int u = 0; u < ST_BATCH; ++u) {
           const int e = e0 + u * ST_THREADS;
-          if (e < later_items && later_row(e))
-            sub4(Pown[(later_first + e / (NF * TPF)) * ST_F * TPF + e % (NF * TPF)], gv[u]);
+          if (e < later_items && later_stage(e) < n_q) sub4(later_part(e), gv[u]);
         }
       }
     }
@@ -534,10 +537,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
 
   // a slice copy whose wait gave up may still be landing: wait (bounded) for it
   if (t == 32) {
-    for (int b = 0; b < NB; ++b) {
+    for (int bb = 0; bb < NB; ++bb) {
       int last = -1;
-      for (int q = b; q < n_q; q += NB) last = q;
-      if (last >= 0) mbar_wait(&cb_full[b], (uint32_t)((last / NB) & 1));
+      for (int q = bb; q < n_q; q += NB) last = q;
+      if (last >= 0) mbar_wait(&cb_full[bb], (uint32_t)((last / NB) & 1));
     }
   }
   cluster_sync_all();  // no CTA leaves while another may still address its shared memory
@@ -646,9 +649,9 @@ cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const f
                                               status);
   if (S.kc == 128)
     return launch_search<kCodeDim, 2, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
-  if (S.kc == 256)
-    return launch_search<kCodeDim, 1, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
-  return launch_search<kCodeDim, 1, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+  if (S.kc % (2 * ST_THREADS) == 0)
+    return launch_search<kCodeDim, 1, 2>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
+  return launch_search<kCodeDim, 1, 1>(cfg, nf_max, p0, cb_s, cn, g, codes, n, dm.K, n_q, NB, dm.metric, status);
 }
 
 }  // namespace rvq

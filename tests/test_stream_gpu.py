@@ -100,10 +100,11 @@ def test_cluster_sizes_and_ragged_counts(N, K):
     check(W, x, label=f"N={N} K={K}")
 
 
-@pytest.mark.parametrize("K,Q", [(2048, 3), (4096, 10)])
+@pytest.mark.parametrize("K,Q", [(2048, 3), (4096, 10), (1152, 2), (2176, 3), (3968, 2)])
 def test_wide_slices(K, Q):
-    """256 and 512 codewords per CTA (one thread per codeword, the second with
-    one slice buffer instead of two)."""
+    """256 and 512 codewords per CTA (one thread per codeword; the second with
+    two codewords a thread and one slice buffer instead of two), and slices of
+    144, 272 and 496 codewords (K/8 not a multiple of 128: some threads idle)."""
     D = 256
     W = weights(D, K, Q, 64, seed=K)
     x = np.random.default_rng(K).standard_normal((40, D)).astype(np.float32)
