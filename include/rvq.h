@@ -78,7 +78,7 @@ extern "C" {
 #endif
 
 #define RVQ_VERSION_MAJOR 0
-#define RVQ_VERSION_MINOR 2
+#define RVQ_VERSION_MINOR 3
 #define RVQ_VERSION_PATCH 0
 
 /* Distance of the argmin (rvq_dims.metric). */

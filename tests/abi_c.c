@@ -53,6 +53,11 @@ int main(void) {
   EXPECT(rvq_status_string(RVQ_ERR_CUDA) != NULL);
   EXPECT(rvq_version() != NULL && strlen(rvq_version()) > 0);
   {
+    char want[32];
+    snprintf(want, sizeof(want), "%d.%d.%d", RVQ_VERSION_MAJOR, RVQ_VERSION_MINOR, RVQ_VERSION_PATCH);
+    EXPECT(strstr(rvq_version(), want) != NULL); /* the string and the header macros agree */
+  }
+  {
     const int64_t prev = rvq_set_stream_max_frames(-1); /* query only */
     EXPECT(prev >= 0);
     EXPECT(rvq_set_stream_max_frames(5) == prev);
