@@ -458,7 +458,7 @@ def per_workload_table(args):
 
 def latency_table(args):
     """Small-batch encode latency for each encode workload: calls of 1, 16 and
-    256 frames on the streaming kernels (the default for calls of up to
+    256 frames (--sizes) on the streaming kernels (the default for calls of up to
     rvq_set_stream_max_frames frames) and, for comparison, on the tile kernels
     (threshold 0).  Per call: CUDA-event time of back-to-back calls on one
     stream, and the median host wall time of a single call with a synchronize
@@ -469,7 +469,7 @@ def latency_table(args):
     dev = torch.device("cuda", 0)
     default = rq.rvq_set_stream_max_frames(-1)
     only = None if args.workload == WORKLOAD else args.workload  # --workload picks one (profiling)
-    sizes = (args.frames,) if args.frames else (1, 16, 256)
+    sizes = (args.frames,) if args.frames else tuple(int(v) for v in args.sizes.split(","))
     for w in ri.WORKLOADS:
         if w.kind == "decode" or (only and w.name != only):
             continue
@@ -544,6 +544,7 @@ def main():
     ap.add_argument("--peaks", action="store_true", help="measure TF32/FP32 GEMM and L2 bandwidths instead")
     ap.add_argument("--table", action="store_true", help="per-workload encode/decode throughput instead")
     ap.add_argument("--latency", action="store_true", help="small-batch encode latency per workload instead")
+    ap.add_argument("--sizes", default="1,16,256", help="frames per call of --latency (comma-separated)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps, always
     if args.peaks:

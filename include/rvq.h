@@ -252,11 +252,13 @@ RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const fl
 /* Small batches.  A call of at most `max_frames` frames (rvq_encode,
  * rvq_reconstruct, rvq_encode_static, and each chunk of a larger call) runs on
  * low-latency kernels: the stage projections spread over many CTAs, then
- * each group of up to 16 frames on one cluster of min(8, K/128) CTAs that
- * each own a slice of every codebook and exchange their best (distance,
- * index) per frame through distributed shared memory, so a call of a few
- * frames finishes in microseconds instead of walking every codeword of every
- * stage on one SM.  It computes the same
+ * groups of up to 16 frames on clusters of min(8, K/128) CTAs that each own
+ * a slice of every codebook and exchange their best (distance, index) per
+ * frame through distributed shared memory, so a call of a few frames
+ * finishes in microseconds instead of walking every codeword of every stage
+ * on one SM.  A cluster takes one group, or, for calls of more than 16
+ * frames, as many groups (up to 8) as put the whole call in one wave of
+ * clusters on the GPU, fewer where its shared memory runs out.  It computes the same
  * codes (distances in float32 FMA; ties to the lowest index) and takes
  * d = 8, or d = 64 with K <= 4096 (and n_q <= 42 when K = 128); other shapes
  * use the tile kernels.  Sets the process-wide threshold (0 turns the small-batch kernel
@@ -264,6 +266,16 @@ RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const fl
  * current value.  The default is 512 frames.  Thread-safe; a change applies to
  * calls made after it. */
 RVQ_API int64_t rvq_set_stream_max_frames(int64_t max_frames);
+
+/* How one call (or one chunk) of n_frames frames at depth n_q would run, for
+ * the current device; launches nothing.  plan (host memory, 6 values):
+ * [0] 1 if the call takes the small-batch kernels, else 0 and the rest 0;
+ * [1] CTAs per cluster; [2] frames per group; [3] groups per cluster;
+ * [4] clusters; [5] codebook slice buffers per CTA.  The first call on a
+ * device asks the CUDA runtime how many clusters fit on it at once; if that
+ * fails, RVQ_ERR_CUDA.  RVQ_ERR_INVALID_ARG (plan untouched) for bad dims,
+ * n_q outside 1..Q, n_frames < 0 or a null plan. */
+RVQ_API rvq_status rvq_stream_plan(rvq_dims dims, int32_t n_q, int64_t n_frames, int64_t *plan);
 
 /* Static strings. */
 RVQ_API const char *rvq_status_string(rvq_status status);

@@ -30,7 +30,7 @@ __all__ = [
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "RVQ_STATIC_SCRATCH_BYTES", "RVQ",
     "EXPORTED_SYMBOLS", "rvq_pipeline_workspace_bytes", "rvq_pipeline_create", "rvq_pipeline_destroy",
-    "rvq_pipeline_reconstruct", "RVQPipeline", "rvq_set_stream_max_frames",
+    "rvq_pipeline_reconstruct", "RVQPipeline", "rvq_set_stream_max_frames", "rvq_stream_plan",
 ]
 
 RVQ_OK = 0
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = [
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "rvq_pipeline_workspace_bytes",
     "rvq_pipeline_create", "rvq_pipeline_destroy", "rvq_pipeline_reconstruct", "rvq_set_stream_max_frames",
+    "rvq_stream_plan",
 ]
 
 RVQ_STATIC_SCRATCH_BYTES = 16 << 20  # include/rvq.h
@@ -104,6 +105,7 @@ def load_library(path: Optional[str] = None):
         "rvq_pipeline_destroy": ([vp], ctypes.c_int),
         "rvq_pipeline_reconstruct": ([vp, vp, vp, i64, vp, vp], ctypes.c_int),
         "rvq_set_stream_max_frames": ([i64], i64),
+        "rvq_stream_plan": ([rvq_dims, i32, i64, ctypes.POINTER(i64)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -235,6 +237,14 @@ def rvq_version() -> str:
 def rvq_set_stream_max_frames(max_frames: int) -> int:
     """Threshold (frames per call) of the small-batch kernel; returns the previous one."""
     return int(load_library().rvq_set_stream_max_frames(int(max_frames)))
+
+
+def rvq_stream_plan(dims: rvq_dims, n_q: int, n_frames: int) -> dict:
+    """How one call of n_frames frames would run on the current device."""
+    out = (ctypes.c_int64 * 6)()
+    _check("rvq_stream_plan", load_library().rvq_stream_plan(dims, int(n_q), int(n_frames), out))
+    keys = ("stream", "cluster_ctas", "group_frames", "groups_per_cluster", "clusters", "slice_buffers")
+    return {k: int(v) for k, v in zip(keys, out)}
 
 
 # ---------------------------------------------------------------------------

@@ -171,6 +171,13 @@ RVQ_API const char *rvq_status_string(rvq_status status) {
   return "unknown status";
 }
 
+RVQ_API rvq_status rvq_stream_plan(rvq_dims dims, int32_t n_q, int64_t n_frames, int64_t *plan) {
+  const rvq_status s = check_dims(dims);
+  if (s != RVQ_OK) return s;
+  if (n_q < 1 || n_q > dims.Q || n_frames < 0 || plan == nullptr) return RVQ_ERR_INVALID_ARG;
+  return rvq::stream_plan(dims, n_q, n_frames, plan) == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA;
+}
+
 RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.3.0 (sm_103a)"; }
 
 }  // extern "C"

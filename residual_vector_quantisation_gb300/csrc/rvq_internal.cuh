@@ -90,14 +90,17 @@ inline const T *at(const void *base, size_t off) {
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t s);
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0,
                                 int64_t n, int n_q, int32_t *codes, float *p0, int *status, cudaStream_t s);
-// The streaming path (rvq_stream.cu): each group of up to kStreamFrames frames
-// runs on one cluster of stream_cluster_size(K) CTAs, each owning K/CS
+// The streaming path (rvq_stream.cu): groups of up to kStreamFrames frames
+// run on clusters of stream_cluster_size(K) CTAs (one or more groups a
+// cluster), each CTA owning K/CS
 // codewords of every stage.  stream_supported: true if it takes a call of
 // n_frames frames at depth n_q (else the tile path does).
 constexpr int kStreamFrames = 16;
 constexpr int kStreamMaxFramesDefault = 512;
 __host__ __device__ inline int stream_cluster_size(int K) { return K / 128 < 8 ? K / 128 : 8; }
 bool stream_supported(const rvq_dims &dm, int n_q, int64_t n_frames);
+// The streaming plan of a call (rvq_stream_plan's six values).
+cudaError_t stream_plan(const rvq_dims &dm, int n_q, int64_t n_frames, int64_t plan[6]);
 // p0: scratch for the stage projections ([n][n_q*d] f32); zero_status: the
 // first kernel clears the status word (the caller has not).
 cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q,

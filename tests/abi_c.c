@@ -65,6 +65,23 @@ int main(void) {
     EXPECT(rvq_set_stream_max_frames(prev) == 5);
     EXPECT(rvq_set_stream_max_frames(-7) == prev);
   }
+  {
+    /* argument checks and the shapes that never take the small-batch kernels
+     * answer without the CUDA runtime */
+    rvq_dims dm = {256, 64, 1024, 8, RVQ_METRIC_L2, 0, 0};
+    int64_t plan[6] = {7, 7, 7, 7, 7, 7};
+    EXPECT(rvq_stream_plan(dm, 0, 16, plan) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_stream_plan(dm, 9, 16, plan) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_stream_plan(dm, 8, -1, plan) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_stream_plan(dm, 8, 16, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(plan[0] == 7 && plan[5] == 7);
+    const int64_t prev = rvq_set_stream_max_frames(100);
+    EXPECT(rvq_stream_plan(dm, 8, 101, plan) == RVQ_OK && plan[0] == 0 && plan[4] == 0);
+    EXPECT(rvq_stream_plan(dm, 8, 0, plan) == RVQ_OK && plan[0] == 0);
+    rvq_set_stream_max_frames(prev);
+    dm.K = 8192; /* d = 64 with K > 4096: tile kernels only */
+    EXPECT(rvq_stream_plan(dm, 8, 16, plan) == RVQ_OK && plan[0] == 0);
+  }
   if (failures == 0) printf("abi_c: ok\n");
   return failures == 0 ? 0 : 1;
 }

@@ -140,6 +140,51 @@ def test_many_groups():
     check(W, x, label="300 frames")
 
 
+@pytest.mark.parametrize("N", [33, 513, 1000, 2500])
+@pytest.mark.parametrize("d,K,Q,metric", [(64, 1024, 8, "l2"), (64, 4096, 3, "l2"), (64, 1024, 32, "l2"),
+                                          (8, 1024, 12, "cosine"), (64, 256, 5, "cosine"), (64, 1152, 4, "l2")])
+def test_several_groups_per_cluster(N, d, K, Q, metric):
+    """Calls of hundreds to thousands of frames: each cluster takes several
+    16-frame groups (as many as put the call in about one wave of clusters,
+    up to 8, fewer where shared memory runs out: 32 stages, K = 4096), the
+    last cluster ragged; 2500 frames take two waves."""
+    D = 128
+    W = weights(D, K, Q, d, seed=N + K + Q, decay=0.9)
+    x = np.random.default_rng(N + d).standard_normal((N, D)).astype(np.float32)
+    check(W, x, metric=metric, label=f"N={N} d={d} K={K} Q={Q} {metric}")
+
+
+def test_plan_of_a_call():
+    """rvq_stream_plan: one group per cluster up to 16 frames (group sizes 1, 2,
+    4, 8, 16 by the call's size); beyond, the fewest groups per cluster (up to
+    8) that put the call in one wave, so that the cluster count falls as the
+    groups per cluster rise; the clusters cover every frame; calls above the
+    threshold or of shapes without the streaming tables take the tile path."""
+    dims = rq._dims(1024, 64, 1024, 8)
+    with stream_max(ALL):
+        for n, nf in ((1, 1), (2, 2), (3, 4), (5, 8), (9, 16), (16, 16)):
+            p = rq.rvq_stream_plan(dims, 8, n)
+            assert p == {"stream": 1, "cluster_ctas": 8, "group_frames": nf, "groups_per_cluster": 1,
+                         "clusters": 1, "slice_buffers": 2}, (n, p)
+        one_wave = None
+        for n in range(17, 16 * 8 * 40, 37):
+            p = rq.rvq_stream_plan(dims, 8, n)
+            G, c = p["groups_per_cluster"], p["clusters"]
+            assert p["stream"] == 1 and p["group_frames"] == 16 and 1 <= G <= 8
+            assert c * 16 * G >= n > (c - 1) * 16 * G, (n, p)
+            if G < 8:  # G - 1 groups would need more clusters than this G's
+                assert -(-n // (16 * (G - 1) if G > 1 else 1)) > c or G == 1, (n, p)
+                one_wave = c if one_wave is None else max(one_wave, c)
+        assert one_wave is not None and one_wave >= 2
+        # a deep stack of wide slices: shared memory caps the groups per cluster
+        deep = rq.rvq_stream_plan(rq._dims(768, 64, 4096, 32), 32, 4096)
+        assert deep["stream"] == 1 and 1 <= deep["groups_per_cluster"] < 8 and deep["slice_buffers"] >= 1
+    with stream_max(100):
+        assert rq.rvq_stream_plan(dims, 8, 101)["stream"] == 0
+        assert rq.rvq_stream_plan(dims, 8, 100)["stream"] == 1
+    assert rq.rvq_stream_plan(rq._dims(256, 64, 8192, 4), 4, 16)["stream"] == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "omnivoice", "moss_deep", "k4096_q10", "moss_lfq", "omnivoice_fc"])
 def test_workload_shapes_small_batches(name):
     """The first frames of each workload, in calls of 1, 16 and 48 frames."""
