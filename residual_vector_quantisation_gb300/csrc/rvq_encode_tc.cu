@@ -36,46 +36,62 @@ using namespace ptx;
 
 // ===========================================================================
 // step 1: P0 = x . w_in^T + b_in
-// CTA item: 256 frames (two M=128 tiles) x 256 output columns, K = D in
-// slices of 16 floats (64-byte rows, 64-byte swizzle), 3-stage TMA ring.
+// CTA item: NT tiles of 128 frames x NC output columns (NT = 2, NC = 256 for
+// large calls; one tile and 128 or 64 columns when a call has too few such
+// items to fill the GPU), K = D in slices of 16 floats (64-byte rows, 64-byte
+// swizzle), 3-stage TMA ring.
 // Warps: 0 and 6 TMA producers (x tiles; w_in hi and lo tiles -- a thread's
 // copies are carried out one after another, so two threads issue them),
 // 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
 // ===========================================================================
 constexpr int PJ_BK = 16;
 constexpr int PJ_STAGES = 3;
-constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;          // 8 KB: one tile's K-slice
-constexpr uint32_t PJ_B = 256 * PJ_BK * 4;               // 16 KB
-constexpr uint32_t PJ_STAGE = 4 * PJ_A_TILE + 2 * PJ_B;  // raw[2] lo[2] bhi blo = 64 KB
-constexpr uint32_t PJ_TX_X = 2 * PJ_A_TILE;             // bytes each producer's TMA writes per stage
-constexpr uint32_t PJ_TX_W = 2 * PJ_B;
+constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;  // 8 KB: one tile's K-slice
 constexpr int PJ_THREADS = 224;
-constexpr uint32_t PJ_IDESC = idesc_tf32(128, 256);
+
+template <int NT, int NC>
+struct PjShape {
+  static constexpr uint32_t B = NC * PJ_BK * 4;                      // one w_in part's K-slice
+  static constexpr uint32_t STAGE = 2 * NT * PJ_A_TILE + 2 * B;      // raw[NT] lo[NT] bhi blo
+  static constexpr uint32_t TX_X = NT * PJ_A_TILE;                   // bytes each producer's TMA writes per stage
+  static constexpr uint32_t TX_W = 2 * B;
+  static constexpr uint32_t TMEM_COLS = NT * NC;
+  static constexpr uint32_t IDESC = idesc_tf32(128, NC);
+  static constexpr int ROWS = 128 * NT;                              // frames per item
+};
 
 struct PjBars {
   uint64_t full[PJ_STAGES], conv[PJ_STAGES], empty[PJ_STAGES];
   uint64_t acc_full, acc_empty, drain;
   uint32_t tmem;
 };
-constexpr size_t PJ_SMEM = 1024 + PJ_STAGES * PJ_STAGE + sizeof(PjBars);
+template <int NT, int NC>
+constexpr size_t pj_smem() { return 1024 + PJ_STAGES * PjShape<NT, NC>::STAGE + sizeof(PjBars); }
 
 __device__ __forceinline__ void record_error(int *status, int code) { atomicCAS(status, 0, code); }
 
+// zero_status: clear the status word first (a call whose first kernel this
+// is); the kernel also lets a dependent launch start at once (programmatic
+// dependent launch; no effect on a plain launch after it).
+template <int NT, int NC>
 __global__ void __launch_bounds__(PJ_THREADS, 1)
     k_project_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_whi,
                  const __grid_constant__ CUtensorMap tm_wlo, const float *__restrict__ bias,
                  float *__restrict__ P0, int64_t n_rows, int n_cols, int D, int n_items, int n_cb,
-                 int *__restrict__ status) {
+                 int *__restrict__ status, int zero_status) {
+  using S = PjShape<NT, NC>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
-  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * PJ_STAGE);
+  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * S::STAGE);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();
+  if (zero_status && blockIdx.x == 0 && tid == 0) *status = 0;
   const int nk = D / PJ_BK;
-  auto a_raw = [&](int s, int t) { return smem + s * PJ_STAGE + t * PJ_A_TILE; };
-  auto a_lo = [&](int s, int t) { return smem + s * PJ_STAGE + (2 + t) * PJ_A_TILE; };
-  auto b_hi = [&](int s) { return smem + s * PJ_STAGE + 4 * PJ_A_TILE; };
-  auto b_lo = [&](int s) { return smem + s * PJ_STAGE + 4 * PJ_A_TILE + PJ_B; };
+  auto a_raw = [&](int s, int t) { return smem + s * S::STAGE + t * PJ_A_TILE; };
+  auto a_lo = [&](int s, int t) { return smem + s * S::STAGE + (NT + t) * PJ_A_TILE; };
+  auto b_hi = [&](int s) { return smem + s * S::STAGE + 2 * NT * PJ_A_TILE; };
+  auto b_lo = [&](int s) { return smem + s * S::STAGE + 2 * NT * PJ_A_TILE + S::B; };
 
   if (tid == 0) {
     for (int s = 0; s < PJ_STAGES; ++s) {
@@ -92,7 +108,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     prefetch_tmap(&tm_wlo);
   }
   if (warp == 1) {
-    tmem_alloc(&bar.tmem, 512);
+    tmem_alloc(&bar.tmem, S::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -107,7 +123,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int m0 = (item / n_cb) * 256, c0 = (item % n_cb) * 256;
+        const int m0 = (item / n_cb) * S::ROWS, c0 = (item % n_cb) * NC;
         for (int ks = 0; ks < nk; ++ks, ++it) {
           const int s = it % PJ_STAGES;
           const uint32_t use = it / PJ_STAGES;
@@ -117,11 +133,11 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
             break;
           }
           if (px) {
-            mbar_arrive_expect_tx(&bar.full[s], PJ_TX_X);
-            tma_load_2d(a_raw(s, 0), &tm_x, ks * PJ_BK, m0, &bar.full[s]);
-            tma_load_2d(a_raw(s, 1), &tm_x, ks * PJ_BK, m0 + 128, &bar.full[s]);
+            mbar_arrive_expect_tx(&bar.full[s], S::TX_X);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) tma_load_2d(a_raw(s, t), &tm_x, ks * PJ_BK, m0 + 128 * t, &bar.full[s]);
           } else {
-            mbar_arrive_expect_tx(&bar.full[s], PJ_TX_W);
+            mbar_arrive_expect_tx(&bar.full[s], S::TX_W);
             tma_load_2d(b_hi(s), &tm_whi, ks * PJ_BK, c0, &bar.full[s]);
             tma_load_2d(b_lo(s), &tm_wlo, ks * PJ_BK, c0, &bar.full[s]);
           }
@@ -154,17 +170,17 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < NT; ++t)
 #pragma unroll
             for (int j = 0; j < PJ_BK / 8; ++j) {
               const uint64_t ah = smem_desc(smem_addr(a_raw(s, t)) + j * 32, 16, 512, kSwizzle64B);
               const uint64_t al = smem_desc(smem_addr(a_lo(s, t)) + j * 32, 16, 512, kSwizzle64B);
               const uint64_t bh = smem_desc(smem_addr(b_hi(s)) + j * 32, 16, 512, kSwizzle64B);
               const uint64_t bl = smem_desc(smem_addr(b_lo(s)) + j * 32, 16, 512, kSwizzle64B);
-              const uint32_t d = tmem + t * 256;
-              mma_tf32(d, ah, bh, PJ_IDESC, (ks | j) ? 1u : 0u);
-              mma_tf32(d, ah, bl, PJ_IDESC, 1u);
-              mma_tf32(d, al, bh, PJ_IDESC, 1u);
+              const uint32_t d = tmem + t * NC;
+              mma_tf32(d, ah, bh, S::IDESC, (ks | j) ? 1u : 0u);
+              mma_tf32(d, ah, bl, S::IDESC, 1u);
+              mma_tf32(d, al, bh, S::IDESC, 1u);
             }
           mma_commit(&bar.empty[s]);
         }
@@ -182,8 +198,8 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     uint32_t it = 0, n_done = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n_done) {
-      const int64_t m0 = (int64_t)(item / n_cb) * 256;
-      const int c0 = (item % n_cb) * 256;
+      const int64_t m0 = (int64_t)(item / n_cb) * S::ROWS;
+      const int c0 = (item % n_cb) * NC;
       for (int ks = 0; ks < nk; ++ks, ++it) {
         const int s = it % PJ_STAGES;
         if (!__all_sync(0xffffffffu, mbar_wait(&bar.full[s], (it / PJ_STAGES) & 1))) {
@@ -191,11 +207,11 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
           ok = false;
           break;
         }
-        // lo = a - trunc_tf32(a), element-wise over both tiles' raw slices
+        // lo = a - trunc_tf32(a), element-wise over the tiles' raw slices
         const float4 *src = reinterpret_cast<const float4 *>(a_raw(s, 0));
         float4 *dst = reinterpret_cast<float4 *>(a_lo(s, 0));
 #pragma unroll
-        for (int u = 0; u < (2 * PJ_A_TILE / 16) / 128; ++u) {
+        for (int u = 0; u < (NT * PJ_A_TILE / 16) / 128; ++u) {
           const float4 v = src[ct + u * 128];
           float4 l;
           l.x = v.x - __uint_as_float(__float_as_uint(v.x) & 0xffffe000u);
@@ -215,13 +231,13 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < NT; ++t) {
         const int64_t n = m0 + t * 128 + r;
         float *out = P0 + n * n_cols + c0;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < NC; c += 32) {
           float v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + t * 256 + c, v);
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + t * NC + c, v);
           tmem_wait_ld();
           if (n < n_rows && c0 + c < n_cols) {
             // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
@@ -246,7 +262,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, S::TMEM_COLS);
   }
 }
 
@@ -820,7 +836,11 @@ cudaError_t ensure_attributes() {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (g_attr_done.load() & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(k_project_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PJ_SMEM);
+  e = cudaFuncSetAttribute(k_project_tc<2, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pj_smem<2, 256>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_project_tc<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pj_smem<1, 128>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_project_tc<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pj_smem<1, 64>());
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_search_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
   if (e != cudaSuccess) return e;
@@ -841,34 +861,65 @@ int sm_count() {
   return v;
 }
 
+// The item shape of the projection: 256 frames x 256 columns, or, when a
+// smaller item (128 x 64, else 128 x 128) puts the whole call in one wave on
+// the SMs, that one -- a call with few frames then spreads over more SMs.
+// (Several waves of small items measured slower than one wave of large ones:
+// 470 against 443 us for 9728 frames of ten 4096-entry stages.)
+int projection_shape(int64_t n, int n_cols, int sms) {
+  const int64_t t128 = (n + 127) / 128;
+  if (t128 * ((n_cols + 63) / 64) <= sms) return 2;
+  if (t128 * ((n_cols + 127) / 128) <= sms) return 1;
+  return 0;
+}
+
 }  // namespace
+
+cudaError_t launch_project_tc(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q, float *p0,
+                              int *status, bool zero_status, cudaStream_t st, int shape) {
+  const TablesLayout L = tables_layout(dm);
+  const int D = dim_in(dm), d = dm.d, Q = dm.Q;  // frames are D_in wide (fc folded into w_in)
+  const int n_cols = n_q * d;
+  cudaError_t e = ensure_attributes();
+  if (e != cudaSuccess) return e;
+  const int sms = sm_count();
+  if (shape < 0) shape = projection_shape(n, n_cols, sms);
+  const uint32_t nc = shape == 0 ? 256 : shape == 1 ? 128 : 64, rows = shape == 0 ? 256 : 128;
+  CUtensorMap tm_x, tm_whi, tm_wlo;
+  if ((e = tensor_map_2d(&tm_x, x, (uint64_t)D, (uint64_t)n, PJ_BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&tm_whi, at<float>(tables, L.w_in_hi), (uint64_t)D, (uint64_t)Q * d, PJ_BK, nc,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+    return e;
+  if ((e = tensor_map_2d(&tm_wlo, at<float>(tables, L.w_in_lo), (uint64_t)D, (uint64_t)Q * d, PJ_BK, nc,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+    return e;
+  const int n_cb = (int)((n_cols + nc - 1) / nc);
+  const int items = (int)((n + rows - 1) / rows) * n_cb;
+  const int grid = items < sms ? items : sms;
+  const float *b_in = at<float>(tables, L.b_in);
+  const int zs = zero_status ? 1 : 0;
+  if (shape == 0)
+    k_project_tc<2, 256><<<grid, PJ_THREADS, pj_smem<2, 256>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+                                                                      items, n_cb, status, zs);
+  else if (shape == 1)
+    k_project_tc<1, 128><<<grid, PJ_THREADS, pj_smem<1, 128>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+                                                                      items, n_cb, status, zs);
+  else
+    k_project_tc<1, 64><<<grid, PJ_THREADS, pj_smem<1, 64>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+                                                                    items, n_cb, status, zs);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0, int64_t n,
                                 int n_q, int32_t *codes, float *p0, int *status, cudaStream_t st) {
   if (stream_supported(dm, n_q, n))  // a small batch: the low-latency cluster kernels
     return launch_encode_stream(dm, tables, x + n0 * dim_in(dm), n, n_q, codes + n0 * n_q, p0, status, false, st);
   const TablesLayout L = tables_layout(dm);
-  const int D = dim_in(dm), d = dm.d, K = dm.K, Q = dm.Q;  // frames are D_in wide (fc folded into w_in)
-  const int n_cols = n_q * d;
-  cudaError_t e = ensure_attributes();
+  const int d = dm.d, K = dm.K;
+  cudaError_t e = launch_project_tc(dm, tables, x + n0 * dim_in(dm), n, n_q, p0, status, false, st, -1);
   if (e != cudaSuccess) return e;
-  CUtensorMap tm_x, tm_whi, tm_wlo;
-  if ((e = tensor_map_2d(&tm_x, x + n0 * D, (uint64_t)D, (uint64_t)n, PJ_BK, 128, CU_TENSOR_MAP_SWIZZLE_64B)) !=
-      cudaSuccess)
-    return e;
-  if ((e = tensor_map_2d(&tm_whi, at<float>(tables, L.w_in_hi), (uint64_t)D, (uint64_t)Q * d, PJ_BK, 256,
-                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
-    return e;
-  if ((e = tensor_map_2d(&tm_wlo, at<float>(tables, L.w_in_lo), (uint64_t)D, (uint64_t)Q * d, PJ_BK, 256,
-                         CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
-    return e;
-  const int n_pairs_rows = (int)((n + 255) / 256);
-  const int n_cb = (n_cols + 255) / 256;
-  const int items1 = n_pairs_rows * n_cb;
   const int sms = sm_count();
-  k_project_tc<<<items1 < sms ? items1 : sms, PJ_THREADS, PJ_SMEM, st>>>(
-      tm_x, tm_whi, tm_wlo, at<float>(tables, L.b_in), p0, n, n_cols, D, items1, n_cb, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (d == kCodeDimSmall)
     return launch_search8(dm, tables, p0, n, n_q, codes + n0 * n_q, status, sms, st);
   const int tiles = (int)((n + 127) / 128);

@@ -88,6 +88,11 @@ inline const T *at(const void *base, size_t off) {
 
 // Launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaStream_t s);
+// P0 = x . w_in'^T + b_in' on the tensor cores (3xTF32) for n frames at depth
+// n_q; shape: the item shape (0: 256 frames x 256 columns, 1: 128 x 128,
+// 2: 128 x 64; -1: chosen for n); zero_status clears the status word first.
+cudaError_t launch_project_tc(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q, float *p0,
+                              int *status, bool zero_status, cudaStream_t st, int shape);
 cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const float *x, int64_t n0,
                                 int64_t n, int n_q, int32_t *codes, float *p0, int *status, cudaStream_t s);
 // The streaming path (rvq_stream.cu): groups of up to kStreamFrames frames

@@ -58,6 +58,14 @@ __device__ __forceinline__ void st_error(int *status, int code) { atomicCAS(stat
 // ===========================================================================
 // k_project_small
 // ===========================================================================
+// Calls whose projection is at least this many multiply-adds (frames x D_in x
+// n_q*d) take the tensor-core projection of the tile path instead
+// (k_project_tc, one wave of 128-frame items): it has a fixed latency of about
+// 20 us, and measured faster from about 2e8 (omnivoice 384 frames, moss_deep
+// 128, moss_lfq 1024).
+#ifndef RVQ_STREAM_TC_PROJECTION_MACS
+#define RVQ_STREAM_TC_PROJECTION_MACS (int64_t(3) << 26)
+#endif
 constexpr int PS_THREADS = 256;
 constexpr int PS_COLS = 8;   // output columns (rows of w_in') per CTA
 constexpr int PS_F = 16;     // frames per CTA
@@ -701,10 +709,15 @@ cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const f
   cudaError_t e = ensure_stream_attributes();
   if (e != cudaSuccess) return e;
   const int D_in = dim_in(dm), n_cols = n_q * dm.d;
-  const int64_t groups = (n + PS_F - 1) / PS_F;
-  k_project_small<<<dim3((unsigned)(n_cols / PS_COLS), (unsigned)groups), PS_THREADS, PS_SMEM, st>>>(
-      x, at<float>(tables, L.w_in_f), at<float>(tables, L.b_in), p0, n, D_in, n_cols, status, zero_status ? 1 : 0);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (n * D_in * n_cols >= RVQ_STREAM_TC_PROJECTION_MACS) {
+    // enough frames for the tensor cores to pay: 128-frame tiles of 3xTF32 MMAs
+    if ((e = launch_project_tc(dm, tables, x, n, n_q, p0, status, zero_status, st, -1)) != cudaSuccess) return e;
+  } else {
+    const int64_t groups = (n + PS_F - 1) / PS_F;
+    k_project_small<<<dim3((unsigned)(n_cols / PS_COLS), (unsigned)groups), PS_THREADS, PS_SMEM, st>>>(
+        x, at<float>(tables, L.w_in_f), at<float>(tables, L.b_in), p0, n, D_in, n_cols, status, zero_status ? 1 : 0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   const int nf = n > 8 ? ST_FG : n > 4 ? 8 : n > 2 ? 4 : (int)n;  // frames per group, >= min(n, 16)
   const int G = stream_groups(dm, n_q, n, stream_cluster_size(dm.K));
