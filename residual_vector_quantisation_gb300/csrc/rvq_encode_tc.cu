@@ -306,12 +306,17 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // two.  (Otherwise a CTA's last item may hold one tile alone; it runs on
 // pipeline 0 with no turns.  It ends no later than the two-tile items of the
 // other CTAs, so splitting it would not shorten the launch.)
+// A launch with no more tiles than the GPU holds clusters of two CTAs (and
+// a multiple of four chunks a stage) runs each tile on a CTA pair instead:
+// the same split item on both SMs of a cluster, each taking half the chunks,
+// so a call of up to about 76 tiles uses all the SMs' tensor cores.
 // ===========================================================================
 constexpr int SR_KC = 128;                    // codewords per chunk (MMA N)
 constexpr uint32_t SR_ATOM = 128 * 128;       // 128 codewords x 128 B
 constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // one bulk copy: hi or lo part of a chunk
 constexpr int SR_SLOTS = 3;                   // half-chunks in the ring
 constexpr int SR_SLOTS_SPLIT = 5;             // ... when every item is split: plus tile 1's two areas
+constexpr int SR_SLOTS_CPAIR = 4;             // ... split across a CTA pair: tile 1's staging area holds the pair's minima
 constexpr int SR_THREADS = 384;
 constexpr uint32_t SR_TMEM_COLS = 512;        // 256 per tile
 constexpr uint32_t SR_TILE_COLS = 256;
@@ -329,6 +334,7 @@ struct SrBars {
   uint64_t turn[2];  // turn[t]: the other tile's issuer has issued most of its chunk
   uint64_t drain[2];
   uint64_t xch_full[2], xch_free[2];  // split items: pipeline 1's stage minima (in TMEM), double-buffered
+  uint64_t px_full[2];                // CTA pairs: the other CTA's stage minima have landed, double-buffered
   uint32_t tmem;
   uint32_t pad;
 };
@@ -338,11 +344,24 @@ static_assert(SR_RING_BYTES + 2 * SR_PART_BYTES == SR_SLOTS_SPLIT * SR_HALF, "sp
 constexpr size_t SR_SMEM = 1024 + SR_RING_BYTES + 4 * SR_PART_BYTES + SR_CN_SLOTS * SR_CN_BYTES + sizeof(SrBars);
 static_assert(SR_SMEM <= 227 * 1024, "search kernel shared memory");
 
-template <bool SPLIT>
+// MODE 0: items of two tiles; 1: one tile per CTA, split between its two
+// pipelines; 2: one tile per cluster of two CTAs (CPAIR), CTA r scanning the
+// chunks c = r mod 2 of each stage with its two pipelines (c / 2 = t mod 2
+// on pipeline t); at the end of a stage each CTA's pipeline 0 sends its
+// per-frame (value, index) minimum to the other CTA's shared memory and both
+// keep the lexicographic minimum of the two, so both hold the same codes and
+// build the same next query.
+template <int MODE>
 __global__ void __launch_bounds__(SR_THREADS, 1)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
                 int n_tiles, int metric, int *__restrict__ status) {
+  constexpr bool SPLIT = MODE >= 1, CPAIR = MODE == 2;
+  // this CTA's item index and the number of such (a CTA pair counts once);
+  // unsigned, like blockIdx.x itself (signed forms measured 2.5 % slower:
+  // more registers spilled in the row threads)
+#define CTA_ID (CPAIR ? (blockIdx.x >> 1) : blockIdx.x)
+#define N_CTA (CPAIR ? (gridDim.x >> 1) : gridDim.x)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -354,18 +373,25 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   // tiles of this CTA: b + 2Bk as tile 0 and b + B + 2Bk as tile 1
   // (b = blockIdx.x, B = gridDim.x); a launch with no more tiles than CTAs
   // thus puts one tile on each SM, split between the CTA's two pipelines
-  const int sweep = 2 * gridDim.x;
+  const int sweep = 2 * N_CTA;
   // Every CTA walks the same codebook chunks; starting each at a different
   // chunk spreads the simultaneous bulk copies over nkc chunks of L2 instead
   // of one hot chunk.  The argmin merge below is order-independent.
-  const int rot = blockIdx.x % nkc;
+  const int rot = CTA_ID % nkc;
   constexpr int d = kCodeDim;
-  constexpr int SLOTS = SPLIT ? SR_SLOTS_SPLIT : SR_SLOTS;
+  constexpr int SLOTS = CPAIR ? SR_SLOTS_CPAIR : SPLIT ? SR_SLOTS_SPLIT : SR_SLOTS;
+  // CTA pairs: this CTA's rank in its cluster; its chunks are c = rank,
+  // rank + 2, ... (in a split item pipeline t takes those with c / 2 = t mod 2)
+  const uint32_t prank = CPAIR ? cluster_ctarank() : 0u;
+  constexpr int C_STEP = CPAIR ? 2 : 1;
   // the split ring takes tile 1's areas: only for launches of one tile per CTA
-  if (SPLIT && (n_tiles > (int)gridDim.x || nkc % 2 != 0)) {
+  if ((SPLIT && (n_tiles > (int)N_CTA || nkc % (CPAIR ? 4 : 2) != 0)) ||
+      (CPAIR && (cluster_nctarank() != 2u || (gridDim.x & 1u) != 0u))) {
     if (threadIdx.x == 0) record_error(status, RVQ_DEVICE_BAD_LAUNCH);
-    return;
+    return;  // uniform over the cluster: no CTA reaches a cluster barrier
   }
+  // CTA pairs: the other CTA's minima, [2][128] (value bits, index)
+  uint2 *px = reinterpret_cast<uint2 *>(smem + SR_RING_BYTES + SR_PART_BYTES);
 
   if (tid == 0) {
     for (int s = 0; s < SLOTS; ++s) {
@@ -384,6 +410,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       mbar_init(&bar.turn[t], 1);
       mbar_init(&bar.xch_full[t], 128);
       mbar_init(&bar.xch_free[t], 128);
+      mbar_init(&bar.px_full[t], 128);  // one remote arrive per frame
     }
     fence_mbar_init();
   }
@@ -394,6 +421,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (CPAIR) cluster_sync_all();  // the other CTA's barriers are initialised before any remote arrive
   const uint32_t tmem = bar.tmem;
 
   if (warp == 0 || warp == 11) {
@@ -405,9 +433,9 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     if (lane == 0) {
       uint32_t ch = 0;  // chunks gone through
       bool ok = true;
-      for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep)
+      for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep)
         for (int q = 0; q < n_q && ok; ++q)
-          for (int c = 0; c < nkc && ok; ++c, ++ch) {
+          for (int c = (int)prank; c < nkc && ok; c += C_STEP, ++ch) {
             const int cr = (c + rot) % nkc;
             const uint32_t j = 2 * ch + (1 - h);
             const int s = j % SLOTS;
@@ -470,20 +498,20 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       const uint64_t desc0 = smem_desc(smem_addr(ring), 16, 1024, kSwizzle128B);
       const uint32_t tb = tmem + t * SR_TILE_COLS;
       const uint32_t ta = SPLIT ? tmem : tb;  // the query's columns
-      for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep) {
-        const bool pair = !SPLIT && t0 + (int)gridDim.x < n_tiles;  // tile 1 present in this item
+      for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep) {
+        const bool pair = !SPLIT && t0 + (int)N_CTA < n_tiles;  // tile 1 present in this item
         if (t == 1 && !pair && !SPLIT) break;
         const bool turns = SPLIT || pair;
         const bool twice = !pair;  // sole user of each half-chunk
         for (int q = 0; q < n_q && ok; ++q, ++builds)
-          for (int c = 0; c < nkc && ok; ++c, ++ch) {
-            if (SPLIT && (c & 1) != t) continue;
+          for (int c = (int)prank; c < nkc && ok; c += C_STEP, ++ch) {
+            if (SPLIT && ((CPAIR ? c >> 1 : c) & 1) != t) continue;
             const uint32_t j0 = 2 * ch, j1 = j0 + 1;  // the chunk's lo and hi half-chunks
             const int s0 = j0 % SLOTS, s1 = j1 % SLOTS;
             // the accumulator free, the query built, the lo half in, the turn: issuer
             // 1's n-th chunk follows issuer 0's n-th, issuer 0's follows issuer 1's (n-1)-th
             if (u > 0 && !wait_or_fail(&bar.acc_empty[t], (u - 1) & 1)) break;
-            if (c == (SPLIT ? t : 0) && !wait_or_fail(&bar.a_ready[SPLIT ? 0 : t], builds & 1)) break;
+            if (c == (CPAIR ? (int)prank + 2 * t : SPLIT ? t : 0) && !wait_or_fail(&bar.a_ready[SPLIT ? 0 : t], builds & 1)) break;
             if (!wait_or_fail(&bar.b_full[s0], (j0 / SLOTS) & 1)) break;
             if (turns && (t == 1 || u > 0) && !wait_or_fail(&bar.turn[t], (t == 1 ? u : u - 1) & 1)) break;
             ++u;
@@ -571,18 +599,19 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       pending = false;
     };
 
-    const int n_cta = gridDim.x;
+    const int n_cta = N_CTA;
     // split items: pipeline 1's (value, index) per frame, two column pairs of
     // its query columns (unused in a split item), in this frame's TMEM lane
     const uint32_t xch = tmem + SR_TILE_COLS + ((uint32_t)(quarter * 32) << 16) + SR_A_HI;
     uint32_t ua = 0, xu = 0, nb = 0;  // accumulator uses, stage minima handed over, queries seen
     float s_row = 1.0f;               // this frame's distance scale (1 / n(p) for the cosine metric)
     // the first query's partial: the projection row itself (tile 1 only if the first item has one)
-    if (tile == 0 || (!SPLIT && blockIdx.x + n_cta < n_tiles)) {
-      const int64_t n = (int64_t)(blockIdx.x + tile * n_cta) * 128 + quarter * 32 + lane;
+    if (tile == 0 || (!SPLIT && CTA_ID + n_cta < n_tiles)) {
+      const int64_t n = (int64_t)(CTA_ID + tile * n_cta) * 128 + quarter * 32 + lane;
       term_issue(P0 + (n < n_rows ? n : 0) * ld, true);
     }
-    for (int t0 = blockIdx.x; t0 < n_tiles && ok; t0 += sweep) {
+    uint32_t xs = 0;  // CTA pairs: stage minima exchanged
+    for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep) {
       const bool pair = !SPLIT && t0 + n_cta < n_tiles;
       constexpr bool split = SPLIT;
       if (tile == 1 && !pair && !split) break;
@@ -594,7 +623,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       const bool has_next = my_tile + sweep < n_tiles;
       // a tile 0 without a partner tile or split releases the norm blocks for both
       const bool alone = !pair && !split;
-      const int n_own = split ? nkc / 2 : nkc;  // chunks scanned per stage
+      const int n_own = CPAIR ? nkc / 4 : split ? nkc / 2 : nkc;  // chunks scanned per stage
       for (int q = 0; q < n_q && ok; ++q) {
         if (!scan_only) {
           // ---- stage boundary: the query = partial - the last known term (if
@@ -688,9 +717,9 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         // ---- scan the K distances ||c||^2 - 2 p.c; keep the lexicographic (value, index) minimum
         float best_v = __int_as_float(0x7f800000);
         int best_k = 0;
-        for (int c = 0; c < nkc; ++c, ++cc) {
+        for (int c = (int)prank; c < nkc; c += C_STEP, ++cc) {
           const int sn = cc % SR_CN_SLOTS;
-          if (split && (c & 1) != tile) {
+          if (split && ((CPAIR ? c >> 1 : c) & 1) != tile) {
             // the other pipeline's chunk: its norm block is released by both, in order
             if (!__all_sync(0xffffffffu, mbar_wait(&bar.cn_full[sn], (cc / SR_CN_SLOTS) & 1))) {
               record_error(status, RVQ_DEVICE_TIMEOUT);
@@ -746,7 +775,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           // ---- this chunk's share of the next query's known terms, in order:
           //      the previous one is added now, the new one stays in flight
           //      until after the next chunk's scan
-          const int target = (n_terms * ((split ? c >> 1 : c) + 1) + n_own - 1) / n_own;
+          const int target = (n_terms * ((CPAIR ? c >> 2 : split ? c >> 1 : c) + 1) + n_own - 1) / n_own;
           for (; done < target; ++done) {
             if (pending) term_finish();
             term_issue(term_row(done), done == 0);
@@ -788,17 +817,43 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             best_k = (int)o_k;
           }
         }
+        if (CPAIR) {
+          // ---- the pair's exchange: this CTA's minimum into the other CTA's
+          //      shared memory (a store, then a release arrive on its barrier),
+          //      then the lexicographic minimum of the two -- the same in both
+          const uint32_t b = xs & 1, other = prank ^ 1u;
+          const int f = quarter * 32 + lane;
+          st_cluster_v2u32(cluster_map(smem_addr(px + b * 128 + f), other), __float_as_uint(best_v), (uint32_t)best_k);
+          mbar_arrive_cluster(cluster_map(smem_addr(&bar.px_full[b]), other));
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(&bar.px_full[b], (xs >> 1) & 1))) {
+            record_error(status, RVQ_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          ++xs;
+          // (buffer b is written again two exchanges later, after the other
+          // CTA has had this CTA's next minimum, sent after this read)
+          const uint2 o = px[b * 128 + f];
+          const float ov = __uint_as_float(o.x);
+          if (ov < best_v || (ov == best_v && (int)o.y < best_k)) {
+            best_v = ov;
+            best_k = (int)o.y;
+          }
+        }
         my_codes[q] = best_k;
-        if (valid) codes[n * n_q + q] = best_k;
+        if (valid && prank == 0) codes[n * n_q + q] = best_k;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (CPAIR) cluster_sync_all();  // no CTA leaves while the other may still write into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, SR_TMEM_COLS);
   }
+#undef CTA_ID
+#undef N_CTA
 }
 
 // ===========================================================================
@@ -842,12 +897,39 @@ cudaError_t ensure_attributes() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_project_tc<1, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pj_smem<1, 64>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_search_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  e = cudaFuncSetAttribute(k_search_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_search_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  e = cudaFuncSetAttribute(k_search_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_search_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SR_SMEM);
   if (e != cudaSuccess) return e;
   g_attr_done.fetch_or(bit);
   return cudaSuccess;
+}
+
+// Clusters of two search CTAs the device holds at once (0 if the query fails).
+int max_pair_clusters() {
+  static std::atomic<int> cached{-1};
+  int v = cached.load();
+  if (v >= 0) return v;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(SR_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SR_SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  v = 0;
+  if (cudaOccupancyMaxActiveClusters(&v, k_search_tc<2>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();  // the query's error is not the caller's
+    v = 0;
+  }
+  cached.store(v);
+  return v;
 }
 
 int sm_count() {
@@ -923,12 +1005,29 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   if (d == kCodeDimSmall)
     return launch_search8(dm, tables, p0, n, n_q, codes + n0 * n_q, status, sms, st);
   const int tiles = (int)((n + 127) / 128);
+  const int nkc = K / SR_KC;
+  const float *G = at<float>(tables, L.g), *cb_img = at<float>(tables, L.cb_img), *cn = at<float>(tables, L.cnorm);
+  int32_t *codes_c = codes + n0 * n_q;
+  if (nkc % 4 == 0 && tiles <= max_pair_clusters()) {
+    // one wave of CTA pairs: each tile's chunks split over two SMs
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(2 * tiles), 1, 1);
+    cfg.blockDim = dim3(SR_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SR_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_search_tc<2>, p0, G, cb_img, cn, codes_c, n, n_q, K, tiles, dm.metric, status);
+  }
   // no more tiles than SMs: every item is split, and the ring takes tile 1's areas
-  auto search = tiles <= sms && (K / SR_KC) % 2 == 0 ? k_search_tc<true> : k_search_tc<false>;
-  search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, at<float>(tables, L.g),
-                                                                 at<float>(tables, L.cb_img),
-                                                                 at<float>(tables, L.cnorm), codes + n0 * n_q, n,
-                                                                 n_q, K, tiles, dm.metric, status);
+  auto search = tiles <= sms && nkc % 2 == 0 ? k_search_tc<1> : k_search_tc<0>;
+  search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, G, cb_img, cn, codes_c, n, n_q, K, tiles,
+                                                                 dm.metric, status);
   return cudaGetLastError();
 }
 
