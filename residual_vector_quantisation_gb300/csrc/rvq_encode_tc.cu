@@ -907,29 +907,51 @@ cudaError_t ensure_attributes() {
   return cudaSuccess;
 }
 
-// Clusters of two search CTAs the device holds at once (0 if the query fails).
-int max_pair_clusters() {
+// Clusters of CS (here 2) search CTAs the device holds at once (0 if the
+// query fails).
+template <int CS>
+int max_search_clusters() {
   static std::atomic<int> cached{-1};
   int v = cached.load();
   if (v >= 0) return v;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3((unsigned)CS, 1, 1);
   cfg.blockDim = dim3(SR_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SR_SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = (unsigned)CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   v = 0;
-  if (cudaOccupancyMaxActiveClusters(&v, k_search_tc<2>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&v, k_search_tc<CS>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();  // the query's error is not the caller's
     v = 0;
   }
   cached.store(v);
   return v;
+}
+
+// One tile per cluster of CS CTAs.
+template <int CS>
+cudaError_t launch_search_clusters(const float *p0, const float *G, const float *cb_img, const float *cn,
+                                   int32_t *codes, int64_t n, int n_q, int K, int tiles, int metric, int *status,
+                                   cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(CS * tiles), 1, 1);
+  cfg.blockDim = dim3(SR_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SR_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_search_tc<CS>, p0, G, cb_img, cn, codes, n, n_q, K, tiles, metric, status);
 }
 
 int sm_count() {
@@ -943,16 +965,28 @@ int sm_count() {
   return v;
 }
 
-// The item shape of the projection: 256 frames x 256 columns, or, when a
-// smaller item (128 x 64, else 128 x 128) puts the whole call in one wave on
-// the SMs, that one -- a call with few frames then spreads over more SMs.
-// (Several waves of small items measured slower than one wave of large ones:
-// 470 against 443 us for 9728 frames of ten 4096-entry stages.)
+// The item shape of the projection: 256 frames x 256 columns, or a smaller
+// item (128 x 128 or 128 x 64) that spreads a call with few frames over more
+// SMs, whichever needs the fewest MMA cycles on the busiest SM (waves x the
+// cycles of an item's K-slice: 12 MMAs of 128 x 256 x 8 at 128 cycles, 6 of
+// 128 x 128 x 8 at 64, 6 of 128 x 64 x 8 at 48), small items in at most two
+// waves: more re-read x and w_in from L2 more often than they save (three
+// waves measured 470 against 443 us for 9728 frames of ten 4096-entry stages).
 int projection_shape(int64_t n, int n_cols, int sms) {
   const int64_t t128 = (n + 127) / 128;
-  if (t128 * ((n_cols + 63) / 64) <= sms) return 2;
-  if (t128 * ((n_cols + 127) / 128) <= sms) return 1;
-  return 0;
+  const int64_t items[3] = {((n + 255) / 256) * ((n_cols + 255) / 256), t128 * ((n_cols + 127) / 128),
+                            t128 * ((n_cols + 63) / 64)};
+  const int64_t slice_cycles[3] = {12 * 128, 6 * 64, 6 * 48};
+  int best = 0;
+  int64_t best_cost = ((items[0] + sms - 1) / sms) * slice_cycles[0];
+  for (int i = 1; i < 3; ++i) {
+    const int64_t waves = (items[i] + sms - 1) / sms;
+    if (waves <= 2 && waves * slice_cycles[i] < best_cost) {
+      best = i;
+      best_cost = waves * slice_cycles[i];
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -1008,22 +1042,9 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   const int nkc = K / SR_KC;
   const float *G = at<float>(tables, L.g), *cb_img = at<float>(tables, L.cb_img), *cn = at<float>(tables, L.cnorm);
   int32_t *codes_c = codes + n0 * n_q;
-  if (nkc % 4 == 0 && tiles <= max_pair_clusters()) {
-    // one wave of CTA pairs: each tile's chunks split over two SMs
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(2 * tiles), 1, 1);
-    cfg.blockDim = dim3(SR_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SR_SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_search_tc<2>, p0, G, cb_img, cn, codes_c, n, n_q, K, tiles, dm.metric, status);
-  }
+  // one wave of CTA pairs: each tile's chunks split over two SMs
+  if (nkc % 4 == 0 && tiles <= max_search_clusters<2>())
+    return launch_search_clusters<2>(p0, G, cb_img, cn, codes_c, n, n_q, K, tiles, dm.metric, status, st);
   // no more tiles than SMs: every item is split, and the ring takes tile 1's areas
   auto search = tiles <= sms && nkc % 2 == 0 ? k_search_tc<1> : k_search_tc<0>;
   search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, G, cb_img, cn, codes_c, n, n_q, K, tiles,

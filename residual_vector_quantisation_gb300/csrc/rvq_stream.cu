@@ -60,7 +60,7 @@ __device__ __forceinline__ void st_error(int *status, int code) { atomicCAS(stat
 // ===========================================================================
 // Calls whose projection is at least this many multiply-adds (frames x D_in x
 // n_q*d) take the tensor-core projection of the tile path instead
-// (k_project_tc, one wave of 128-frame items): it has a fixed latency of about
+// (k_project_tc in 128-frame items): it has a fixed latency of about
 // 20 us, and measured faster from about 2e8 (omnivoice 384 frames, moss_deep
 // 128, moss_lfq 1024).
 #ifndef RVQ_STREAM_TC_PROJECTION_MACS

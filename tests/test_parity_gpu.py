@@ -208,6 +208,24 @@ def test_pair_and_split_items_mixed(cta_rounds, extra, K, metric):
     run_small(W, x, label=f"tiles={cta_rounds}x{sms}+{extra} K={K} {metric}", metric=metric)
 
 
+@pytest.mark.parametrize("K,Q,N,metric", [(4096, 3, 1, "l2"), (4096, 3, 1000, "l2"), (2048, 4, 4000, "cosine"),
+                                          (4096, 2, 4900, "l2"), (1024, 5, 700, "l2"), (512, 3, 130, "cosine"),
+                                          (1024, 3, 9000, "l2")])
+def test_tiles_on_clusters(K, Q, N, metric):
+    """Calls that fit one wave of 2-CTA clusters (and have a multiple of four
+    128-codeword chunks a stage: K = 512 .. 4096) run each 128-frame tile on a
+    cluster pair splitting every stage's codebook chunks and exchanging
+    per-frame minima through distributed shared memory.  The tile kernels are
+    forced (threshold 0); every frame is checked."""
+    prev = rq.rvq_set_stream_max_frames(0)
+    try:
+        w, W = _small_weights(D=96, K=K, Q=Q, seed=K + N, bias=True)
+        x = np.random.default_rng(K + N).standard_normal((N, 96)).astype(np.float32)
+        run_small(W, x, label=f"K={K} Q={Q} N={N} {metric}", metric=metric)
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
+
+
 def test_biases_and_prefix_depths():
     w, W = _small_weights(D=256, K=512, Q=6, bias=True)
     x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
