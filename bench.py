@@ -38,9 +38,10 @@ import rvq_inputs as ri  # noqa: E402
 
 WORKLOAD = "large_batch"
 METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of k_project_tc (209.7 MB)
-# and k_search_tc<0> (94.9 MB) over 38 912 frames of large_batch.
-ENCODE_DRAM_BYTES_PER_FRAME = {"large_batch": (209.7e6 + 94.9e6) / 38912}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of k_project_tc<2, 256>
+# (167.7 + 42.1 MB) and k_search_tc<0> (91.3 + 0.5 MB) over 38 912 frames of
+# large_batch (the same kernels as the full workload's, one wave).
+ENCODE_DRAM_BYTES_PER_FRAME = {"large_batch": (209.8e6 + 91.9e6) / 38912}
 L2_BYTES = 129 * 2 ** 20
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
