@@ -241,16 +241,19 @@ __device__ __forceinline__ void sub4(float4 &p, const float4 g) {
 // whole call has fewer); CW: codewords a thread scores together (2 when kc is
 // a multiple of 512, sharing the loads of the frames' projections; otherwise a
 // thread takes codewords kk, kk + 256, ... one at a time, and kc need not be a
-// multiple of 256).
-template <int d, int SPLITJ, int NF, int CW>
+// multiple of 256).  MULTI: several groups a cluster (G_arg of them); without
+// it G = 1 at compile time, so that the one-group kernel of the smallest calls
+// keeps its constant trip counts.
+template <int d, int SPLITJ, int NF, int CW, bool MULTI>
 __global__ void __launch_bounds__(ST_THREADS, 1)
     k_stream_search(const float *__restrict__ P0, const float4 *__restrict__ cb_s, const float *__restrict__ cnorm,
                     const float4 *__restrict__ g, int32_t *__restrict__ codes, int64_t n, int K, int n_q, int NB,
-                    int G, int metric, int *__restrict__ status) {
+                    int G_arg, int metric, int *__restrict__ status) {
   constexpr int TPF = d / 4;            // float4 columns of a row of d
   constexpr int DJ4 = TPF / SPLITJ;     // float4 columns of a codeword per thread
   constexpr unsigned kRedMask = 16 * NF >= 32 ? 0xffffffffu : 0x0000ffffu;
   extern __shared__ __align__(128) unsigned char smem[];
+  const int G = MULTI ? G_arg : 1;      // groups per cluster
   const int FPC = NF * G;               // frames per cluster
   const int NU = (FPC + 1) / 2;         // 16-byte units of FPC keys
   const int FPX = 2 * NU;               // stride of a rank's keys in xch
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const int CS = S.CS, kc = S.kc;
   if (cluster_nctarank() != (uint32_t)CS || blockDim.x != ST_THREADS || dynamic_smem_size() < S.total ||
       (SPLITJ == 2) != (kc == 128) || (CW == 2 && kc % (2 * ST_THREADS) != 0) || (NB != 1 && NB != 2 && NB != 3) ||
-      G < 1 || G > ST_MAX_G || (G > 1 && NF != ST_FG) || (NF < ST_FG && n > NF)) {
+      G_arg < 1 || G_arg > ST_MAX_G || (MULTI ? NF != ST_FG : G_arg != 1) || (NF < ST_FG && n > NF)) {
     griddep_wait();  // after the projection kernel, which may clear the status word
     if (t == 0) st_error(status, RVQ_DEVICE_BAD_LAUNCH);
     return;  // uniform over the cluster: no CTA reaches a cluster barrier
@@ -579,11 +582,12 @@ cudaError_t set_search_attrs() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ST_SMEM_LIMIT);
   };
-  set(k_stream_search<d, SPLITJ, 1, CW>);
-  set(k_stream_search<d, SPLITJ, 2, CW>);
-  set(k_stream_search<d, SPLITJ, 4, CW>);
-  set(k_stream_search<d, SPLITJ, 8, CW>);
-  set(k_stream_search<d, SPLITJ, 16, CW>);
+  set(k_stream_search<d, SPLITJ, 1, CW, false>);
+  set(k_stream_search<d, SPLITJ, 2, CW, false>);
+  set(k_stream_search<d, SPLITJ, 4, CW, false>);
+  set(k_stream_search<d, SPLITJ, 8, CW, false>);
+  set(k_stream_search<d, SPLITJ, 16, CW, false>);
+  set(k_stream_search<d, SPLITJ, 16, CW, true>);
   return e;
 }
 
@@ -608,22 +612,25 @@ template <int d, int SPLITJ, int CW>
 cudaError_t launch_search(cudaLaunchConfig_t &cfg, int nf, const float *p0, const float4 *cb_s, const float *cn,
                           const float4 *g, int32_t *codes, int64_t n, int K, int n_q, int NB, int G, int metric,
                           int *status) {
+  if (G > 1)
+    return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16, CW, true>, p0, cb_s, cn, g, codes, n, K, n_q, NB,
+                              G, metric, status);
   switch (nf) {
     case 1:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 1, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB, G,
-                                metric, status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 1, CW, false>, p0, cb_s, cn, g, codes, n, K, n_q,
+                                NB, G, metric, status);
     case 2:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 2, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB, G,
-                                metric, status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 2, CW, false>, p0, cb_s, cn, g, codes, n, K, n_q,
+                                NB, G, metric, status);
     case 4:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 4, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB, G,
-                                metric, status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 4, CW, false>, p0, cb_s, cn, g, codes, n, K, n_q,
+                                NB, G, metric, status);
     case 8:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 8, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB, G,
-                                metric, status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 8, CW, false>, p0, cb_s, cn, g, codes, n, K, n_q,
+                                NB, G, metric, status);
     default:
-      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16, CW>, p0, cb_s, cn, g, codes, n, K, n_q, NB, G,
-                                metric, status);
+      return cudaLaunchKernelEx(&cfg, k_stream_search<d, SPLITJ, 16, CW, false>, p0, cb_s, cn, g, codes, n, K, n_q,
+                                NB, G, metric, status);
   }
 }
 
@@ -653,7 +660,7 @@ int max_active_clusters(int CS) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int nc = 0;
-  if (cudaOccupancyMaxActiveClusters(&nc, k_stream_search<kCodeDim, 1, 16, 1>, &cfg) == cudaSuccess && nc > 0)
+  if (cudaOccupancyMaxActiveClusters(&nc, k_stream_search<kCodeDim, 1, 16, 1, true>, &cfg) == cudaSuccess && nc > 0)
     v = nc;
   else
     (void)cudaGetLastError();  // the query's error is not the caller's
