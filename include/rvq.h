@@ -235,8 +235,9 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *pipeline, const void *
 /* Encode like rvq_encode, but with no scratch argument: for callers that
  * cannot allocate device memory when they encode (a real-time audio callback,
  * where cudaMalloc may stall on device-wide synchronisation, or an application
- * whose device memory all belongs to its own pool).  The pages have no
- * counterpart to this entry point.
+ * whose device memory all belongs to its own pool).  Neither omnivoice.cpp
+ * ARCHITECTURE.md nor moss-tts.cpp AGENTS.md has a counterpart to this entry
+ * point.
  * Scratch is a fixed RVQ_STATIC_SCRATCH_BYTES array inside the library, held
  * on every GPU that loads it until the process exits.  A call needs
  * 256 + n_frames * n_q * d * 4 bytes of it; a larger call returns RVQ_ERR_WORKSPACE

@@ -21,7 +21,7 @@
 // AGENTS.md, gotcha 8).  Using the first n_q of Q stages is the bitrate
 // control of moss-tts.cpp AGENTS.md, gotcha 12.
 //
-// Readings where the pages are silent:
+// Readings where omnivoice.cpp ARCHITECTURE.md and moss-tts.cpp AGENTS.md are silent:
 //   * ties in the argmin go to the lowest index (strict '<' in an ascending scan);
 //   * biases are optional (a null pointer means zero);
 //   * distances are taken in direct form, sum_j (e_j - c_j)^2, in float64;

@@ -13,7 +13,7 @@
 // so a raw float32 tile serves as a_hi) and a_lo = a - a_hi exact in float32;
 // a.b ~= a_hi.b_hi + a_hi.b_lo + a_lo.b_hi, accumulated in float32 in TMEM.
 // That keeps the distances at about float32 accuracy; one TF32 pass (10-bit
-// mantissa) would not (the pages keep the codec in F32 because reduced
+// mantissa) would not (the codec is kept in F32 because reduced
 // precision loses late-codebook matches: omnivoice.cpp ARCHITECTURE.md,
 // "Model conversion").
 //

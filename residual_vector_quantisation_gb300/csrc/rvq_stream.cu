@@ -28,7 +28,7 @@
 //                     into its shared memory, counted by an mbarrier's
 //                     transaction bytes; the smallest key is the code --
 //                     distance first, then the lowest index, as the plain
-//                     argmin of the pages;
+//                     argmin;
 //       update        p_{q+1} -= G[q+1][q][code_q] in every CTA (the
 //                     cross-stage table of rvq_prepare).  The owner of stage
 //                     q+2 applies the same term for it and pushes that stage's

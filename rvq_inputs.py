@@ -108,8 +108,9 @@ WORKLOADS = [
     Workload("decode_only", 64, 750, 1024, 8, 1024, 64, "decode", seed=BASE_SEED + 2),
     Workload("moss_deep", 32, 375, 768, 32, 1024, 64, "gauss", cb_decay=0.8, seed=BASE_SEED + 3),
     Workload("large_batch", 256, 750, 1024, 8, 1024, 64, "planted", sigma=0.2, seed=BASE_SEED + 4),
-    # ten books of 4096 entries (the pages' Audio8 codec); the latent sizes D, d
-    # are not given there, so D=1024, d=64 as in the other shapes
+    # ten books of 4096 entries (the Audio8 codec, audio.cpp
+    # docs/models/audio8_tts.md); the latent sizes D, d are not given there,
+    # so D=1024, d=64 as in the other shapes
     Workload("k4096_q10", 16, 750, 1024, 10, 4096, 64, "planted", sigma=0.05, seed=BASE_SEED + 5),
     # the MOSS tokenizer's quantizer: 32 books of 1024 entries, argmin between
     # L2-normalised vectors in an 8-dim code space (moss-tts.cpp AGENTS.md,

@@ -1,8 +1,9 @@
 """Writes oracle_tiny_regression.json: the float64 oracle's codes and relative
 gaps for the first 24 frames of the 250-frame, D=256, Q=8, K=1024, d=64
 workload (with small biases).  It calls only oracle/ and the input generator.
-The pages print no worked numeric RVQ example, so this fixture pins the oracle
-against unintended change (and across CPU architectures), not against the pages.
+omnivoice.cpp ARCHITECTURE.md and moss-tts.cpp AGENTS.md print no worked
+numeric RVQ example, so this fixture pins the oracle against unintended change
+(and across CPU architectures), not against a printed example.
 
 Run:  python tests/golden/make_golden.py
 """
