@@ -40,9 +40,10 @@
  *
  * Memory and ownership.  Every pointer except the struct pointers is DEVICE
  * memory owned by the caller.  The library allocates nothing, frees nothing
- * and never synchronises the stream: each call validates its arguments on the
- * host, enqueues kernels on `stream` and returns.  Results are ready when the
- * stream reaches that point.
+ * and never synchronises the stream (except rvq_read_status,
+ * rvq_read_error_count and the synchronous host pipeline): each call
+ * validates its arguments on the host, enqueues kernels on `stream` and
+ * returns.  Results are ready when the stream reaches that point.
  *   tables  -- written by rvq_prepare, read-only afterwards; the weights are
  *              not read again, so they may be freed after rvq_prepare's work
  *              has completed on its stream.  One tables buffer may serve
@@ -57,6 +58,10 @@
  *   RVQ_ERR_UNSUPPORTED  shapes the kernels do not handle (see
  *                        rvq_dims_supported);
  *   RVQ_ERR_CUDA         a launch failed (cudaGetLastError after launch).
+ * Failures found on the device after a call has returned (a bounded device
+ * wait that gave up: RVQ_ERR_TIMEOUT; a kernel that refused its launch shape:
+ * RVQ_ERR_INTERNAL) are recorded in the status word at the head of the encode
+ * scratch and read with rvq_read_status; the host pipeline reads them itself.
  * n_frames == 0 is valid and enqueues nothing.  Inputs must be finite; the
  * result for NaN or Inf inputs is unspecified.  Codes given to rvq_decode
  * outside [0, K) contribute nothing and are counted (see rvq_decode).
@@ -78,7 +83,7 @@ extern "C" {
 #endif
 
 #define RVQ_VERSION_MAJOR 0
-#define RVQ_VERSION_MINOR 3
+#define RVQ_VERSION_MINOR 4
 #define RVQ_VERSION_PATCH 0
 
 /* Distance of the argmin (rvq_dims.metric). */
@@ -91,7 +96,9 @@ typedef enum rvq_status {
   RVQ_ERR_UNSUPPORTED = -2,
   RVQ_ERR_WORKSPACE = -3,
   RVQ_ERR_CUDA = -4,
-  RVQ_ERR_TIMEOUT = -5
+  RVQ_ERR_TIMEOUT = -5,
+  RVQ_ERR_CANCELLED = -6,
+  RVQ_ERR_INTERNAL = -7
 } rvq_status;
 
 /* D: the quantizer's input (residual) dimension; d: code-space dimension;
@@ -202,6 +209,26 @@ RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const floa
                                    int64_t n_frames, int32_t n_q, int32_t *codes, float *x_hat,
                                    void *scratch, size_t scratch_bytes, rvq_stream_t stream);
 
+/* Status of the encode work last enqueued with `scratch` (the scratch buffer
+ * given to rvq_encode or rvq_reconstruct; NULL reads the library's own scratch
+ * on the current device, the one rvq_encode_static uses).  Synchronises
+ * `stream` (the stream of that call), then reads the status word at the head
+ * of the scratch: RVQ_OK when that call's kernels ran cleanly,
+ * RVQ_ERR_TIMEOUT when one of their bounded device waits gave up and
+ * RVQ_ERR_INTERNAL when a kernel refused its launch shape -- either way the
+ * call's codes are invalid.  RVQ_ERR_INVALID_ARG for a scratch pointer that
+ * is not 16-byte aligned, RVQ_ERR_CUDA if synchronising or reading fails.
+ * This is the one entry point besides the host pipeline that waits for the
+ * GPU.  (Omnivoice.cpp ARCHITECTURE.md, "Status codes": every failure is
+ * reported as a status value, none is left to be inferred.) */
+RVQ_API rvq_status rvq_read_status(const void *scratch, rvq_stream_t stream);
+
+/* Read the bad-code counter of rvq_decode (`bad_codes`, device int64,
+ * 8-byte aligned) into *n_bad_codes (host) after synchronising `stream`.
+ * RVQ_ERR_INVALID_ARG for a null or misaligned pointer, RVQ_ERR_CUDA if the
+ * synchronisation or the copy fails. */
+RVQ_API rvq_status rvq_read_error_count(const int64_t *bad_codes, int64_t *n_bad_codes, rvq_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Host-memory pipeline: frames in host memory in, codes and reconstruction in
  * host memory out.  The frames are processed in chunks of chunk_frames
@@ -211,6 +238,10 @@ RVQ_API rvq_status rvq_reconstruct(rvq_dims dims, const void *tables, const floa
  * (pinned host memory lets the copies run at full speed).  The pipeline owns
  * three CUDA streams and nine events on the device that was current at
  * creation; it allocates no memory.  One pipeline serves one call at a time.
+ * The first 256 bytes of the workspace hold the pipeline's status word: each
+ * chunk's device status is folded into it, and rvq_pipeline_reconstruct
+ * returns RVQ_ERR_TIMEOUT or RVQ_ERR_INTERNAL if any chunk's kernels recorded
+ * a failure (see rvq_read_status).
  * --------------------------------------------------------------------------- */
 typedef struct rvq_pipeline rvq_pipeline;
 
@@ -228,9 +259,27 @@ RVQ_API rvq_status rvq_pipeline_destroy(rvq_pipeline *pipeline);
 
 /* Encode and decode n_frames host frames x_host [N][D_in] with the tables of
  * rvq_prepare: codes_host [N][n_q] (required) and x_hat_host [N][D_out]
- * (nullable).  Synchronous: returns when every output is in host memory. */
+ * (nullable).  Synchronous: returns when every output is in host memory.
+ * Returns RVQ_ERR_TIMEOUT / RVQ_ERR_INTERNAL if a chunk's kernels recorded a
+ * device failure (its outputs are then invalid), and RVQ_ERR_CANCELLED if the
+ * cancel callback asked to stop. */
 RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *pipeline, const void *tables, const float *x_host,
                                             int64_t n_frames, int32_t *codes_host, float *x_hat_host);
+
+/* Cancel callback of a pipeline: returns non-zero to stop.  As in the public
+ * API of omnivoice.cpp ARCHITECTURE.md ("Public API": a cancel callback the
+ * library polls between chunks), rvq_pipeline_reconstruct calls it on the
+ * calling thread before it enqueues each chunk.  When it returns non-zero, no
+ * further chunk is enqueued: the call waits for the chunks already enqueued
+ * (their codes and reconstructions are written in full), leaves the outputs
+ * of the later frames untouched and returns RVQ_ERR_CANCELLED.  `user` is
+ * passed through. */
+typedef int (*rvq_cancel_fn)(void *user);
+
+/* Install (fn non-NULL) or remove (fn NULL) the pipeline's cancel callback.
+ * RVQ_ERR_INVALID_ARG for a null pipeline.  Not to be called while a
+ * rvq_pipeline_reconstruct on the same pipeline is running. */
+RVQ_API rvq_status rvq_pipeline_set_cancel(rvq_pipeline *pipeline, rvq_cancel_fn fn, void *user);
 
 /* Encode like rvq_encode, but with no scratch argument: for callers that
  * cannot allocate device memory when they encode (a real-time audio callback,
@@ -242,9 +291,12 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *pipeline, const void *
  * on every GPU that loads it until the process exits.  A call needs
  * 256 + n_frames * n_q * d * 4 bytes of it; a larger call returns RVQ_ERR_WORKSPACE
  * before launching anything (split the frames over several calls).  The
- * first call on each device looks up the array's device address, so make it
- * before any stream capture.  All calls share the array: calls that can
- * overlap on the GPU race and must not be issued.  Allocates nothing. */
+ * first call on each device (and the first after the device's context
+ * changes, e.g. after cudaDeviceReset) looks up the array's device address,
+ * so make it before any stream capture.  All calls share the array: calls
+ * that can overlap on the GPU race and must not be issued.  The status word
+ * of the last call (a device wait that gave up, say) is read with
+ * rvq_read_status(NULL, stream).  Allocates nothing. */
 #define RVQ_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 RVQ_API rvq_status rvq_encode_static(rvq_dims dims, const void *tables, const float *x,
                                      int64_t n_frames, int32_t n_q, int32_t *codes,

@@ -31,19 +31,27 @@ __all__ = [
     "rvq_status_string", "rvq_version", "rvq_encode_static", "RVQ_STATIC_SCRATCH_BYTES", "RVQ",
     "EXPORTED_SYMBOLS", "rvq_pipeline_workspace_bytes", "rvq_pipeline_create", "rvq_pipeline_destroy",
     "rvq_pipeline_reconstruct", "RVQPipeline", "rvq_set_stream_max_frames", "rvq_stream_plan",
+    "rvq_read_status", "rvq_read_error_count", "rvq_pipeline_set_cancel", "RVQ_CANCEL_FN",
 ]
 
 RVQ_OK = 0
 STATUS_NAMES = {0: "RVQ_OK", -1: "RVQ_ERR_INVALID_ARG", -2: "RVQ_ERR_UNSUPPORTED",
-                -3: "RVQ_ERR_WORKSPACE", -4: "RVQ_ERR_CUDA", -5: "RVQ_ERR_TIMEOUT"}
+                -3: "RVQ_ERR_WORKSPACE", -4: "RVQ_ERR_CUDA", -5: "RVQ_ERR_TIMEOUT",
+                -6: "RVQ_ERR_CANCELLED", -7: "RVQ_ERR_INTERNAL"}
+RVQ_ERR_TIMEOUT = -5
+RVQ_ERR_CANCELLED = -6
+RVQ_ERR_INTERNAL = -7
 
 EXPORTED_SYMBOLS = [
     "rvq_dims_supported", "rvq_tables_bytes", "rvq_prepare", "rvq_encode_scratch_bytes",
     "rvq_encode_min_scratch_bytes", "rvq_encode", "rvq_decode", "rvq_reconstruct",
     "rvq_status_string", "rvq_version", "rvq_encode_static", "rvq_pipeline_workspace_bytes",
     "rvq_pipeline_create", "rvq_pipeline_destroy", "rvq_pipeline_reconstruct", "rvq_set_stream_max_frames",
-    "rvq_stream_plan",
+    "rvq_stream_plan", "rvq_read_status", "rvq_read_error_count", "rvq_pipeline_set_cancel",
 ]
+
+# int (*rvq_cancel_fn)(void *user)
+RVQ_CANCEL_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p)
 
 RVQ_STATIC_SCRATCH_BYTES = 16 << 20  # include/rvq.h
 
@@ -106,6 +114,9 @@ def load_library(path: Optional[str] = None):
         "rvq_pipeline_reconstruct": ([vp, vp, vp, i64, vp, vp], ctypes.c_int),
         "rvq_set_stream_max_frames": ([i64], i64),
         "rvq_stream_plan": ([rvq_dims, i32, i64, ctypes.POINTER(i64)], ctypes.c_int),
+        "rvq_read_status": ([vp, vp], ctypes.c_int),
+        "rvq_read_error_count": ([vp, ctypes.POINTER(i64), vp], ctypes.c_int),
+        "rvq_pipeline_set_cancel": ([vp, RVQ_CANCEL_FN, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -224,6 +235,27 @@ def _host_ptr(t: Optional[torch.Tensor]):
 def rvq_pipeline_reconstruct(pipeline, tables, x_host, codes_host, x_hat_host=None) -> None:
     _check("rvq_pipeline_reconstruct", load_library().rvq_pipeline_reconstruct(
         pipeline, _ptr(tables), _host_ptr(x_host), x_host.shape[0], _host_ptr(codes_host), _host_ptr(x_hat_host)))
+
+
+def rvq_read_status(scratch: Optional[torch.Tensor] = None, stream=None) -> int:
+    """Synchronise `stream` and return the status (an rvq_status value, not
+    raised) that the encode last enqueued with `scratch` left in its status
+    word; scratch=None reads the library's own scratch (rvq_encode_static)."""
+    return int(load_library().rvq_read_status(_ptr(scratch), _stream(stream)))
+
+
+def rvq_read_error_count(bad_codes: torch.Tensor, stream=None) -> int:
+    """Synchronise `stream` and return rvq_decode's bad-code counter."""
+    out = ctypes.c_int64(0)
+    _check("rvq_read_error_count", load_library().rvq_read_error_count(_ptr(bad_codes), ctypes.byref(out),
+                                                                       _stream(stream)))
+    return int(out.value)
+
+
+def rvq_pipeline_set_cancel(pipeline, fn, user=None) -> None:
+    """fn: an RVQ_CANCEL_FN (the caller keeps it alive) or None to remove."""
+    _check("rvq_pipeline_set_cancel", load_library().rvq_pipeline_set_cancel(
+        pipeline, fn if fn is not None else RVQ_CANCEL_FN(), user))
 
 
 def rvq_status_string(status: int) -> str:
@@ -351,6 +383,11 @@ class RVQPipeline:
         with torch.cuda.device(self.rvq.device):
             rvq_pipeline_reconstruct(self.handle, self.rvq.tables, x_host, codes_host, x_hat_host)
         return codes_host, x_hat_host
+
+    def set_cancel(self, should_stop=None):
+        """should_stop() -> bool is polled before each chunk; None removes it."""
+        self._cancel = None if should_stop is None else RVQ_CANCEL_FN(lambda _user: 1 if should_stop() else 0)
+        rvq_pipeline_set_cancel(self.handle, self._cancel)
 
     def close(self):
         if getattr(self, "handle", None) is not None:

@@ -2,7 +2,8 @@
 //
 // Every entry point validates its arguments on the host before touching the
 // CUDA runtime, so the early-return paths work on a machine with no GPU.
-// Nothing here allocates, frees or synchronises.
+// Nothing here allocates or frees; only the two readers (rvq_read_status,
+// rvq_read_error_count) synchronise a stream.
 #include <stdint.h>
 
 #include "rvq_internal.cuh"
@@ -167,6 +168,8 @@ RVQ_API const char *rvq_status_string(rvq_status status) {
     case RVQ_ERR_WORKSPACE: return "workspace too small";
     case RVQ_ERR_CUDA: return "CUDA launch failed";
     case RVQ_ERR_TIMEOUT: return "device wait timed out";
+    case RVQ_ERR_CANCELLED: return "cancelled";
+    case RVQ_ERR_INTERNAL: return "internal error (a kernel refused its launch shape)";
   }
   return "unknown status";
 }
@@ -178,6 +181,34 @@ RVQ_API rvq_status rvq_stream_plan(rvq_dims dims, int32_t n_q, int64_t n_frames,
   return rvq::stream_plan(dims, n_q, n_frames, plan) == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA;
 }
 
-RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.3.0 (sm_103a)"; }
+RVQ_API rvq_status rvq_read_status(const void *scratch, rvq_stream_t stream) {
+  if (scratch && !aligned16(scratch)) return RVQ_ERR_INVALID_ARG;
+  const void *word_at = scratch;
+  if (!word_at) {
+    void *p = nullptr;
+    if (rvq::static_scratch_address(&p) != cudaSuccess) return RVQ_ERR_CUDA;
+    word_at = p;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  // ordered after the encode on its stream, then waited for
+  if (cudaMemcpyAsync(&word, word_at, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return RVQ_ERR_CUDA;
+  return rvq::status_from_word(word);
+}
+
+RVQ_API rvq_status rvq_read_error_count(const int64_t *bad_codes, int64_t *n_bad_codes, rvq_stream_t stream) {
+  if (!bad_codes || !n_bad_codes || (reinterpret_cast<uintptr_t>(bad_codes) & 7u)) return RVQ_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int64_t v = 0;
+  if (cudaMemcpyAsync(&v, bad_codes, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return RVQ_ERR_CUDA;
+  *n_bad_codes = v;
+  return RVQ_OK;
+}
+
+RVQ_API const char *rvq_version(void) { return "rvq-gb300 0.4.0 (sm_103a)"; }
 
 }  // extern "C"

@@ -44,6 +44,7 @@ struct TablesLayout {
                    //   each 128-codeword chunk as two 128-byte-swizzled K-major atoms
   size_t z;        // [Q][K][D_out] f32 decode table (fc2 folded in)
   size_t b_dec;    // [D_out]   f32 decode bias (fc2_b, zeros without fc2)
+  size_t b_dec_used;  // int32: 1 if the decode bias holds fc2_b, 0 if it is all zeros
   size_t g;        // [P][K][d] f32 cross-stage table, P = Q(Q-1)/2
   size_t m64;      // [P][d][d] f64 w_in[q] . w_out[s]   (prepare temporary)
   size_t vb64;     // [P][d]    f64 w_in[q] . b_out[s]   (prepare temporary)
@@ -68,6 +69,7 @@ inline TablesLayout tables_layout(const rvq_dims &dm) {
   L.cb_img = take(Q * K * d * 2 * 4);
   L.z = take(Q * K * Do * 4);
   L.b_dec = take(Do * 4);
+  L.b_dec_used = take(4);
   L.g = take((P ? P : 1) * K * d * 4);
   L.m64 = take((P ? P : 1) * d * d * 8);
   L.vb64 = take((P ? P : 1) * d * 8);
@@ -114,5 +116,15 @@ cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *
                            int32_t *codes, int *status, int sms, cudaStream_t s);
 cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t *codes, int64_t n,
                           int n_q, float *y, int64_t *bad, cudaStream_t s);
+
+// The status a device status word stands for (0: RVQ_OK, RVQ_DEVICE_TIMEOUT:
+// RVQ_ERR_TIMEOUT, anything else: RVQ_ERR_INTERNAL).
+inline rvq_status status_from_word(int word) {
+  if (word == 0) return RVQ_OK;
+  return word == RVQ_DEVICE_TIMEOUT ? RVQ_ERR_TIMEOUT : RVQ_ERR_INTERNAL;
+}
+// Device address, in the current context, of the library's own encode scratch
+// (rvq_encode_noalloc.cu).
+cudaError_t static_scratch_address(void **out);
 
 }  // namespace rvq

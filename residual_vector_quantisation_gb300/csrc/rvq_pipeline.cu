@@ -5,6 +5,14 @@
 // copy of one chunk, the encode + decode of the previous one, and the
 // device-to-host copy of the one before that; events order the slots.  The
 // pipeline object owns only those streams and events; it allocates no memory.
+//
+// Failures: each chunk's encode clears and may set the status word of its
+// slot's scratch; a one-thread kernel on the compute stream folds it into the
+// pipeline's own status word (the head of the workspace) before the slot is
+// reused, so a device wait that gave up in any chunk is reported when the
+// call returns.  A cancel callback is polled between chunks (omnivoice.cpp
+// ARCHITECTURE.md, "Public API": generation takes a cancel callback that the
+// library polls, so a long job can be stopped between steps).
 #include <new>
 
 #include "rvq_internal.cuh"
@@ -12,6 +20,13 @@
 namespace {
 
 constexpr int kSlots = 3;
+constexpr size_t kPipeHeader = 256;  // the pipeline's status word
+
+// Keep the first failure: *acc = *chunk_status unless *acc already holds one.
+__global__ void k_fold_status(int *acc, const int *chunk_status) {
+  const int w = *chunk_status;
+  if (w != 0 && *acc == 0) *acc = w;
+}
 
 struct SlotLayout {
   size_t x, y, codes, scratch, scratch_bytes, stride;
@@ -41,13 +56,15 @@ struct rvq_pipeline {
   SlotLayout layout;
   cudaStream_t s_in, s_comp, s_out;
   cudaEvent_t ev_in[kSlots], ev_comp[kSlots], ev_out[kSlots];
+  rvq_cancel_fn cancel;
+  void *cancel_user;
 };
 
 extern "C" {
 
 RVQ_API size_t rvq_pipeline_workspace_bytes(rvq_dims dims, int32_t n_q, int64_t chunk_frames) {
   if (rvq_dims_supported(dims) != RVQ_OK || n_q < 1 || n_q > dims.Q || chunk_frames < 1) return 0;
-  return kSlots * slot_layout(dims, n_q, chunk_frames).stride;
+  return kPipeHeader + kSlots * slot_layout(dims, n_q, chunk_frames).stride;
 }
 
 RVQ_API rvq_status rvq_pipeline_create(rvq_dims dims, int32_t n_q, int64_t chunk_frames, void *workspace,
@@ -115,13 +132,18 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *p, const void *tables,
   const SlotLayout &L = p->layout;
   int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(p->device) != cudaSuccess) return RVQ_ERR_CUDA;
-  rvq_status status = RVQ_OK;
+  int *fold = reinterpret_cast<int *>(p->workspace);
+  rvq_status status = cudaMemsetAsync(fold, 0, sizeof(int), p->s_comp) == cudaSuccess ? RVQ_OK : RVQ_ERR_CUDA;
   const int64_t n_chunks = (n_frames + p->chunk - 1) / p->chunk;
   for (int64_t i = 0; i < n_chunks && status == RVQ_OK; ++i) {
     const int slot = (int)(i % kSlots);
     const int64_t n0 = i * p->chunk;
     const int64_t n = (n_frames - n0 < p->chunk) ? n_frames - n0 : p->chunk;
-    unsigned char *base = p->workspace + slot * L.stride;
+    if (p->cancel && p->cancel(p->cancel_user)) {
+      status = RVQ_ERR_CANCELLED;
+      break;
+    }
+    unsigned char *base = p->workspace + kPipeHeader + slot * L.stride;
     float *x_d = reinterpret_cast<float *>(base + L.x);
     float *y_d = reinterpret_cast<float *>(base + L.y);
     int32_t *c_d = reinterpret_cast<int32_t *>(base + L.codes);
@@ -141,7 +163,9 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *p, const void *tables,
     status = rvq_reconstruct(dm, tables, x_d, n, n_q, c_d, y_d, scratch, L.scratch_bytes,
                              reinterpret_cast<rvq_stream_t>(p->s_comp));
     if (status != RVQ_OK) break;
-    ok = cudaEventRecord(p->ev_comp[slot], p->s_comp) == cudaSuccess;
+    k_fold_status<<<1, 1, 0, p->s_comp>>>(fold, static_cast<const int *>(scratch));
+    ok = cudaGetLastError() == cudaSuccess;
+    ok = ok && cudaEventRecord(p->ev_comp[slot], p->s_comp) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(p->s_out, p->ev_comp[slot], 0) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(codes_host + n0 * n_q, c_d, (size_t)n * n_q * sizeof(int32_t), cudaMemcpyDeviceToHost,
                                p->s_out) == cudaSuccess;
@@ -153,10 +177,25 @@ RVQ_API rvq_status rvq_pipeline_reconstruct(rvq_pipeline *p, const void *tables,
   }
   // the outputs are in host memory when the call returns
   if (cudaStreamSynchronize(p->s_in) != cudaSuccess || cudaStreamSynchronize(p->s_comp) != cudaSuccess ||
-      cudaStreamSynchronize(p->s_out) != cudaSuccess)
+      cudaStreamSynchronize(p->s_out) != cudaSuccess) {
     status = RVQ_ERR_CUDA;
+  } else if (status == RVQ_OK || status == RVQ_ERR_CANCELLED) {
+    // a device failure in any enqueued chunk outranks a cancel
+    int word = 0;
+    if (cudaMemcpy(&word, fold, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      status = RVQ_ERR_CUDA;
+    else if (word != 0)
+      status = rvq::status_from_word(word);
+  }
   if (prev >= 0) cudaSetDevice(prev);
   return status;
+}
+
+RVQ_API rvq_status rvq_pipeline_set_cancel(rvq_pipeline *p, rvq_cancel_fn fn, void *user) {
+  if (!p) return RVQ_ERR_INVALID_ARG;
+  p->cancel = fn;
+  p->cancel_user = fn ? user : nullptr;
+  return RVQ_OK;
 }
 
 }  // extern "C"

@@ -131,10 +131,12 @@ __global__ void k_prep_cb_stream(const float *__restrict__ cb, float *__restrict
   out[e] = (float)((double)cb[row * d + 4 * jb + c] / codeword_divisor(cb + row * d, d, metric));
 }
 
-// The decode bias: fc2_b, or zeros.
-__global__ void k_prep_b_dec(const float *__restrict__ fc2_b, float *__restrict__ b_dec, int D_out) {
+// The decode bias: fc2_b, or zeros; and whether decode needs to add it.
+__global__ void k_prep_b_dec(const float *__restrict__ fc2_b, float *__restrict__ b_dec, int D_out,
+                             int *__restrict__ b_dec_used) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < D_out) b_dec[i] = fc2_b ? fc2_b[i] : 0.0f;
+  if (i == 0) *b_dec_used = fc2_b ? 1 : 0;
 }
 
 // Squared norms of the codewords as the distance uses them (float64 sums).
@@ -299,7 +301,8 @@ void launch_tables(const rvq_dims &dm, const rvq_weights &w, void *tables, cudaS
     k_prep_z<d, float><<<dim3((D + 255) / 256, (unsigned)(rows / 16)), 256, 0, st>>>(w.w_out, w.b_out, w.codebook,
                                                                                      at<float>(tables, L.z), D, K);
   }
-  k_prep_b_dec<<<(D_out + 255) / 256, 256, 0, st>>>(w.fc2_b, at<float>(tables, L.b_dec), D_out);
+  k_prep_b_dec<<<(D_out + 255) / 256, 256, 0, st>>>(w.fc2_b, at<float>(tables, L.b_dec), D_out,
+                                                     at<int>(tables, L.b_dec_used));
   if (P > 0) {
     k_prep_m<d><<<dim3((unsigned)P, d), (d + 31) / 32 * 32 + 32, 0, st>>>(w.w_in, w.w_out, w.b_out, at<double>(tables, L.m64),
                                                          at<double>(tables, L.vb64), D, Q);

@@ -82,6 +82,38 @@ int main(void) {
     dm.K = 8192; /* d = 64 with K > 4096: tile kernels only */
     EXPECT(rvq_stream_plan(dm, 8, 16, plan) == RVQ_OK && plan[0] == 0);
   }
+  {
+    /* the no-allocation encode refuses bad calls before any CUDA call */
+    rvq_dims dm = {1024, 64, 1024, 8, RVQ_METRIC_L2, 0, 0};
+    const void *tab = (const void *)(uintptr_t)0x100000;   /* never dereferenced */
+    const float *x = (const float *)(uintptr_t)0x200000;
+    int32_t *codes = (int32_t *)(uintptr_t)0x300000;
+    EXPECT(rvq_encode_static(dm, NULL, x, 10, 8, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, NULL, 10, 8, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, x, 10, 8, NULL, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, x, 10, 0, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, x, 10, 9, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, x, -1, 8, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, NULL, NULL, 0, 8, NULL, NULL) == RVQ_OK); /* empty batch */
+    EXPECT(rvq_encode_static(dm, (const void *)(uintptr_t)0x100010, x, 10, 8, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, (const float *)(uintptr_t)0x200004, 10, 8, codes, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_encode_static(dm, tab, x, 10, 8, (int32_t *)(uintptr_t)0x300008, NULL) == RVQ_ERR_INVALID_ARG);
+    /* (16 MiB - 256) / (8 * 64 * 4) = 8191 frames fit; 8192 do not */
+    EXPECT(rvq_encode_static(dm, tab, x, 8192, 8, codes, NULL) == RVQ_ERR_WORKSPACE);
+    EXPECT(rvq_encode_static(bad_d, tab, x, 10, 8, codes, NULL) == RVQ_ERR_UNSUPPORTED);
+  }
+  {
+    /* the readers and the cancel hook check their pointers first */
+    int64_t n = 0;
+    EXPECT(rvq_read_error_count(NULL, &n, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_read_error_count((const int64_t *)(uintptr_t)0x100000, NULL, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_read_error_count((const int64_t *)(uintptr_t)0x100004, &n, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_read_status((const void *)(uintptr_t)0x100008, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(rvq_pipeline_set_cancel(NULL, NULL, NULL) == RVQ_ERR_INVALID_ARG);
+    EXPECT(strcmp(rvq_status_string(RVQ_ERR_CANCELLED), "cancelled") == 0);
+    EXPECT(strcmp(rvq_status_string(RVQ_ERR_TIMEOUT), "device wait timed out") == 0);
+    EXPECT(rvq_status_string(RVQ_ERR_INTERNAL) != NULL && strcmp(rvq_status_string(RVQ_ERR_INTERNAL), "unknown status") != 0);
+  }
   if (failures == 0) printf("abi_c: ok\n");
   return failures == 0 ? 0 : 1;
 }

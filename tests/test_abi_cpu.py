@@ -77,6 +77,24 @@ def test_early_return_paths(lib_path):
     assert lib.rvq_encode(ok, fake, fake, 1000, 8, fake, fake, 1000, None) == -1
     # misaligned pointers are rejected
     assert lib.rvq_decode(ok, fake, ctypes.c_void_p((1 << 20) + 4), 5, 8, fake, None, None) == -1
+    # the no-allocation encode: host refusals before any CUDA call
+    a, x, c = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    assert lib.rvq_encode_static(ok, a, x, 0, 8, c, None) == 0
+    assert lib.rvq_encode_static(ok, None, x, 10, 8, c, None) == -1
+    assert lib.rvq_encode_static(ok, a, x, 10, 9, c, None) == -1
+    assert lib.rvq_encode_static(ok, a, ctypes.c_void_p((2 << 20) + 8), 10, 8, c, None) == -1
+    assert lib.rvq_encode_static(ok, a, x, 8192, 8, c, None) == -3            # 16 MiB holds 8191 frames
+    d8 = rq.rvq_dims(768, 8, 1024, 32, rq.RVQ_METRIC_COSINE)
+    assert lib.rvq_encode_static(d8, a, x, (rq.RVQ_STATIC_SCRATCH_BYTES - 256) // (32 * 8 * 4) + 1, 32, c,
+                                 None) == -3
+    # status readers and the pipeline's cancel hook
+    n = ctypes.c_int64(0)
+    assert lib.rvq_read_error_count(None, ctypes.byref(n), None) == -1
+    assert lib.rvq_read_error_count(ctypes.c_void_p((1 << 20) + 4), ctypes.byref(n), None) == -1
+    assert lib.rvq_read_status(ctypes.c_void_p((1 << 20) + 8), None) == -1
+    assert lib.rvq_pipeline_set_cancel(None, rq.RVQ_CANCEL_FN(), None) == -1
+    assert rq.rvq_status_string(-6) == "cancelled"
+    assert rq.rvq_status_string(-5) == "device wait timed out"
     assert rq.rvq_status_string(-4) == "CUDA launch failed"
     assert "sm_103a" in rq.rvq_version()
 

@@ -49,3 +49,14 @@ def test_bounded_wait_times_out_and_context_survives(tmp_path):
     assert torch.equal(after.cpu(), torch.arange(1000, 1032, dtype=torch.int32))
     # and torch's own kernels still run on this context
     assert float((torch.ones(1024, device="cuda") * 2).sum().item()) == 2048.0
+    # the word the timed-out kernel left is what the library's status query
+    # reports for a scratch buffer holding it: RVQ_ERR_TIMEOUT
+    import residual_vector_quantisation_gb300 as rq
+    rqb.build_library()
+    scratch = torch.zeros(64, dtype=torch.int32, device="cuda")
+    scratch[0] = status[0]
+    assert rq.rvq_read_status(scratch) == rq.RVQ_ERR_TIMEOUT
+    scratch[0] = 6  # a kernel that refused its launch shape
+    assert rq.rvq_read_status(scratch) == rq.RVQ_ERR_INTERNAL
+    scratch[0] = 0
+    assert rq.rvq_read_status(scratch) == 0

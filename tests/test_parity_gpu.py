@@ -276,6 +276,7 @@ def test_decode_counts_bad_codes():
     bad = torch.zeros(1, dtype=torch.int64, device=DEV)
     y = rvq.decode(torch.from_numpy(codes).to(DEV), bad_codes=bad).cpu().numpy()
     assert int(bad.item()) == 3
+    assert rq.rvq_read_error_count(bad) == 3  # the same counter through the C ABI reader
     y_ref, n_bad = oracle.decode(W, codes)
     assert n_bad == 3
     assert max_abs_rel_to_rms(y, y_ref, 1.0) <= 1e-5

@@ -73,3 +73,28 @@ def test_pipeline_rejects_bad_arguments(rvq):
     with pytest.raises(ValueError):
         pipe.reconstruct(torch.zeros((4, rvq.D), device=DEV))  # device tensor is not a host buffer
     pipe.close()
+
+
+def test_pipeline_cancel_between_chunks(rvq):
+    """The cancel callback is polled before each chunk (omnivoice.cpp
+    ARCHITECTURE.md, "Public API"): stopping after the first chunk returns
+    RVQ_ERR_CANCELLED with that chunk's outputs written in full and the later
+    frames' outputs untouched; with the callback removed the pipeline runs to
+    the end again."""
+    n, chunk = 1000, 256
+    x = torch.from_numpy(np.random.default_rng(11).standard_normal((n, rvq.D)).astype(np.float32)).pin_memory()
+    pipe = rq.RVQPipeline(rvq, chunk_frames=chunk)
+    want, _ = pipe.reconstruct(x, want_x_hat=False)
+    polls = []
+    pipe.set_cancel(lambda: polls.append(1) or len(polls) > 1)
+    codes = torch.full((n, rvq.Q), -7, dtype=torch.int32).pin_memory()
+    with pytest.raises(rq.RVQError) as err:
+        pipe.reconstruct(x, codes_host=codes, want_x_hat=False)
+    assert err.value.status == rq.RVQ_ERR_CANCELLED
+    assert len(polls) == 2
+    assert torch.equal(codes[:chunk], want[:chunk])
+    assert bool((codes[chunk:] == -7).all())
+    pipe.set_cancel(None)
+    again, _ = pipe.reconstruct(x, want_x_hat=False)
+    assert torch.equal(again, want)
+    pipe.close()

@@ -6,8 +6,11 @@ rvq_encode_static uses a fixed scratch array inside the library instead of a
 caller-provided scratch buffer.  These tests call it through the C ABI and
 check that its codes equal rvq_encode's on two calls in a row (the second call
 must not be disturbed by what the first left in the shared array), that the
-second call changes the device's free memory not at all, and that a call too
-large for the array is refused before anything runs.
+second call changes the device's free memory not at all, that a call too
+large for the array is refused before anything runs, that the status word of
+the last call can be read back (rvq_read_status with no scratch), and that the
+codes follow the float64 oracle on the 8-dim cosine code space and on
+4096-entry codebooks too.
 
 This file is collected last on purpose, so that a run that stops at the first
 failure has already run every other test.
@@ -17,7 +20,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import rvq_inputs as ri
+from rvq_compare import compare_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +64,7 @@ def test_static_scratch_matches_rvq_encode_on_two_calls(prepared):
     for g, w_ in zip(got, want):
         # same kernels and arithmetic as rvq_encode: the codes agree exactly
         assert torch.equal(g, w_)
+    assert rq.rvq_read_status(None) == 0  # the library's own status word: no device wait gave up
 
 
 def test_static_scratch_prefix_depth(prepared):
@@ -81,3 +87,28 @@ def test_static_scratch_refuses_calls_that_do_not_fit(prepared):
     # exactly at the limit is accepted
     rq.rvq_encode_static(rvq.dims, rvq.tables, big[:n_max].contiguous(), rvq.Q, codes[:n_max])
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name,n", [("moss_lfq", 700), ("k4096_q10", 300)])
+def test_static_scratch_other_shapes_against_oracle(name, n):
+    """The 8-dim cosine code space (moss_lfq, its own search kernel) and
+    4096-entry codebooks (k4096_q10): equal to rvq_encode, and the codes follow
+    the oracle under the relative-gap rule, on two calls in a row."""
+    rqb.build_library()
+    w = ri.WORKLOAD_BY_NAME[name]
+    Wn = ri.make_weights(w)
+    W = ri.weights_to_torch(Wn, DEV)
+    rvq = rq.RVQ(W["w_in"], W["codebook"], W["w_out"], device=DEV, metric=w.metric)
+    xn = ri.make_x(w, Wn, rows=np.arange(n))
+    x = torch.from_numpy(xn).to(DEV)
+    ref = oracle.encode(Wn, xn, want_residual=False, metric=w.metric)
+    for part in (slice(0, n), slice(n // 3, n)):
+        xs = x[part].contiguous()
+        got = torch.full((xs.shape[0], w.Q), -7, dtype=torch.int32, device=DEV)
+        rq.rvq_encode_static(rvq.dims, rvq.tables, xs, w.Q, got)
+        want = rvq.encode(xs)
+        torch.cuda.synchronize()
+        assert rq.rvq_read_status(None) == 0
+        assert torch.equal(got, want)
+        res = compare_codes(got.cpu().numpy(), ref["codes"][part], ref["gap"][part])
+        assert res["n_fail"] == 0, res
