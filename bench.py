@@ -38,10 +38,24 @@ import rvq_inputs as ri  # noqa: E402
 
 WORKLOAD = "large_batch"
 METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of k_project_tc<2, 256>
-# (167.7 + 42.1 MB) and k_search_tc<0> (91.3 + 0.5 MB) over 38 912 frames of
-# large_batch (the same kernels as the full workload's, one wave).
-ENCODE_DRAM_BYTES_PER_FRAME = {"large_batch": (209.8e6 + 91.9e6) / 38912}
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per frame of
+# one call, each with the sha256 (first 16 hex digits) of the kernel source it
+# was taken with: a figure whose source has changed since is reported as null.
+# Encode: a one-wave capture (38 912 frames; the traffic follows the frame
+# count); decode: a capture of the full workload (its DRAM counters take one
+# ncu pass).  The profile files hold the commands and the figures.
+TRAFFIC = {
+    ("encode", "large_batch"): {
+        "bytes_per_frame": (167.62e6 + 42.57e6 + 91.36e6 + 0.58e6) / 38912,
+        "source": "residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu",
+        "sha16": "96d467b51046a69a",
+        "profile": "profiles/encode_tc_large_batch.md"},
+    ("decode", "large_batch"): {
+        "bytes_per_frame": (52.42e6 + 738.95e6) / 192000,  # the full workload (one pass)
+        "source": "residual_vector_quantisation_gb300/csrc/rvq_decode.cu",
+        "sha16": "eaf30fea13b8b140",
+        "profile": "profiles/decode_large_batch.md"},
+}
 L2_BYTES = 129 * 2 ** 20
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
@@ -54,6 +68,21 @@ def _peaks():
         return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
                 "sm_max_mhz": p.get("sm_max_mhz", 2070.0), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def source_sha16(rel: str) -> str:
+    import hashlib
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_per_frame(op: str, workload: str):
+    """DRAM bytes per frame from the committed capture, or None when there is
+    none for this workload or the kernel source has changed since."""
+    t = TRAFFIC.get((op, workload))
+    if not t or t["bytes_per_frame"] is None or source_sha16(t["source"]) != t["sha16"]:
+        return None
+    return t["bytes_per_frame"]
 
 
 def encode_flops_per_frame(w) -> float:
@@ -273,10 +302,11 @@ def e2e_time(args, rvq, x, codes, y, stream, barrier, world, dev):
 def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, clocks, world):
     peaks = _peaks()
     clk = clocks.summary()
-    # DRAM bytes (read + write) per frame of one encode call, k_project_tc +
-    # k_search_tc, from one ncu capture of a one-wave case of this workload,
-    # scaled by frames; None for other workloads or once the kernels change.
-    enc_traffic = ENCODE_DRAM_BYTES_PER_FRAME.get(w.name)
+    # DRAM bytes (read + write) per frame of one call, from one ncu capture of
+    # a one-wave case of this workload, scaled by frames; None for other
+    # workloads or once the kernel source has changed since the capture.
+    enc_traffic = traffic_per_frame("encode", w.name)
+    dec_traffic = traffic_per_frame("decode", w.name)
     # encode: 3xTF32 tensor-core kernels.  The TF32 peak is the measured bf16
     # peak times the nominal dense tf32/bf16 ratio (1.1 / 2.25 PFLOP/s); three
     # TF32 passes make up one float32-accurate product, so the roofline for the
@@ -316,7 +346,8 @@ def report(args, w, W, x, N, n_q, ms_step, enc_ms, dec_ms, e2e_ms, scratch, cloc
                      "peak_basis": f"{peaks['source']} bf16 {peaks['bf16_tflops']:.1f} x 1.1/2.25 (tf32) / 3 passes",
                      "frac_of_single_pass_tf32": enc_achieved / tf32_peak},
         "roofline_decode": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": dec_achieved / peaks["hbm_gbs"], "traffic": None,
+                            "frac": dec_achieved / peaks["hbm_gbs"],
+                            "traffic": None if dec_traffic is None else dec_traffic * N,
                             "peak_basis": f"{peaks['source']} HBM copy bandwidth"},
         "cpu_baseline": cpu,
         "e2e": None if e2e_ms is None else {
@@ -408,7 +439,16 @@ def per_workload_table(args):
                      fc_b=Wt.get("fc_b"), fc2_w=Wt.get("fc2_w"), fc2_b=Wt.get("fc2_b"))
         n_q = w.Q
         row = {"workload": w.name, "N": w.N, "D": w.D, "Q": w.Q, "K": w.K, "d": w.d, "metric": w.metric,
-               "D_in": w.D_in, "D_out": w.D_out}
+               "D_in": w.D_in, "D_out": w.D_out, "tables_mb": rvq.tables.numel() / 1e6}
+        # the one-time cost of rvq_prepare for this weight set (warm: after the
+        # constructor's own call), CUDA events
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rq.rvq_prepare(rvq.dims, Wt["w_in"], Wt["codebook"], Wt["w_out"], None, None, rvq.tables,
+                       fc_w=Wt.get("fc_w"), fc_b=Wt.get("fc_b"), fc2_w=Wt.get("fc2_w"), fc2_b=Wt.get("fc2_b"))
+        b.record()
+        torch.cuda.synchronize()
+        row["prepare_ms"] = a.elapsed_time(b)
         if w.kind == "decode":
             codes = torch.from_numpy(ri.make_codes(w)).to(dev)
             x_host = None

@@ -34,6 +34,9 @@ inline int dim_out(const rvq_dims &dm) { return dm.D_out > 0 ? dm.D_out : dm.D; 
 // d = 64 with slices of at most 512 codewords (K <= 4096).
 inline bool stream_tables(const rvq_dims &dm) { return dm.d != kCodeDim || dm.K <= 4096; }
 
+// Blocks of the d = 8 norm operand per stage: one per pair of 128-codeword chunks.
+__host__ __device__ constexpr size_t cn_img8_blocks(int K) { return (size_t)(K / 128 + 1) / 2; }
+
 // Byte offsets of the prepared tables inside the caller's tables buffer.
 struct TablesLayout {
   size_t w_in_hi;  // [Q*d][D_in]  f32, TF32-truncated high part of w_in (. fc_w)
@@ -53,6 +56,9 @@ struct TablesLayout {
   size_t cb_stream;  // [Q][CS][d/4][K/CS] float4: the codebook (each codeword divided by n(c) for the
                      //   cosine metric) cut into the streaming path's CS = stream_cluster_size(K) slices,
                      //   each slice column-block major so one bulk copy stages it
+  size_t cn_img8;  // d = 8 only: [Q][ceil(K/256)][sw32(128 rows x 8)] f32: the squared norms as the
+                   //   B operand of one more MMA -- row k % 128 of the block of chunks 2i, 2i+1 holds
+                   //   the exact TF32 parts (n1, n2, n3) of ||c||^2 in slots 0-2 (even chunk) or 4-6
   size_t total;
 };
 
@@ -77,6 +83,7 @@ inline TablesLayout tables_layout(const rvq_dims &dm) {
   const bool st = stream_tables(dm);  // the streaming copies, else empty
   L.w_in_f = take(st ? Q * d * Di * 4 : 0);
   L.cb_stream = take(st ? Q * K * d * 4 : 0);
+  L.cn_img8 = take(d == (size_t)kCodeDimSmall ? Q * cn_img8_blocks(dm.K) * 128 * 8 * 4 : 0);
   L.total = o;
   return L;
 }

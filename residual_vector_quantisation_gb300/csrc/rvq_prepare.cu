@@ -195,6 +195,32 @@ __global__ void k_prep_cb_img8(const float *__restrict__ cb, float *__restrict__
   img[(chunk + 1) * (128 * d) + off] = lo;
 }
 
+// The d = 8 search's norm operand: ||c||^2 (as rounded once into cnorm) split
+// into three TF32 parts n1 = tf32(n), n2 = tf32(n - n1), n3 = n - n1 - n2,
+// whose sum is n exactly, in the sw32 layout of a 128 x 8 B block:
+// [q][chunk pair][sw32(row = k % 128, slot)], slots 0-2 for the even chunk of
+// the pair and 4-6 for the odd one, zeros elsewhere.  An MMA of this block
+// with A rows [1 1 1 0 0 0 0 0] (even) or [0 0 0 0 1 1 1 0] (odd) adds the
+// chunk's norms to its distances.
+__global__ void k_prep_cn_img8(const float *__restrict__ cnorm, float *__restrict__ img, int K, int64_t n) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // over Q * blocks * 128 * 8
+  if (e >= n) return;
+  const int slot = (int)(e & 7), kk = (int)((e >> 3) & 127);
+  const int64_t qb = e >> 10;  // q * blocks + pair
+  const int64_t blocks = (int64_t)cn_img8_blocks(K);
+  const int q = (int)(qb / blocks), pair = (int)(qb % blocks);
+  const int c = 2 * pair + (slot >> 2);  // chunk
+  float v = 0.0f;
+  if ((slot & 3) < 3 && c < K / kChunkCodes) {
+    const float nrm = cnorm[(int64_t)q * K + c * kChunkCodes + kk];
+    const float n1 = tf32_trunc(nrm);
+    const float n2 = tf32_trunc(nrm - n1);
+    const float n3 = (nrm - n1) - n2;
+    v = (slot & 3) == 0 ? n1 : (slot & 3) == 1 ? n2 : n3;
+  }
+  img[qb * (128 * 8) + ptx::sw32_offset(kk, slot) / 4] = v;
+}
+
 // Z[q][k][i] = sum_j w_out[q][i][j] codebook[q][k][j] + b_out[q][i]  (f64);
 // with fc2 the same with M2, v2 of width D_out for w_out, b_out.
 // grid: (ceil(D/256), Q*K/16); each block handles 16 codewords of one stage.
@@ -344,6 +370,9 @@ cudaError_t launch_prepare(const rvq_dims &dm, const rvq_weights &w, void *table
   } else {
     k_prep_cb_img8<<<(unsigned)((ncb + 255) / 256), 256, 0, st>>>(w.codebook, at<float>(tables, L.cb_img), K, ncb,
                                                                   dm.metric);
+    const int64_t nn = (int64_t)Q * (int64_t)cn_img8_blocks(K) * 128 * 8;
+    k_prep_cn_img8<<<(unsigned)((nn + 255) / 256), 256, 0, st>>>(at<float>(tables, L.cnorm),
+                                                                  at<float>(tables, L.cn_img8), K, nn);
     launch_tables<kCodeDimSmall>(dm, w, tables, st);
   }
   return cudaGetLastError();

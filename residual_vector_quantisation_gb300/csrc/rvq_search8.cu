@@ -10,11 +10,12 @@
 // of the distances by the row threads.  The kernel is laid out for that:
 //   * a stage's whole codebook image (K codewords of -2c, normalised for the
 //     cosine metric, as TF32 hi and lo in 32-byte swizzled 128-codeword
-//     blocks) and its K norms come in by one bulk copy each and stay in
-//     shared memory for the stage, double-buffered by stage;
+//     blocks) and its norm operand (one 4 KB block per pair of chunks) come in
+//     by one bulk copy each and stay in shared memory for the stage,
+//     double-buffered by stage;
 //   * three pipelines per CTA, each four row warps (one thread per frame of a
 //     128-frame tile), one MMA issuer and 160 TMEM columns: query hi [0,8),
-//     query lo [8,16), distances [32,160);
+//     query lo [8,16), the norm MMA's A operands [16,32), distances [32,160);
 //   * with more tiles than SMs each pipeline works on a tile of its own
 //     (items of three tiles); otherwise (the SPLIT variant) the three share
 //     one tile, pipeline p scanning the chunks c = p mod 3, and pipelines 1
@@ -26,9 +27,14 @@
 // folded into an 8-float partial in registers one chunk later, in the order
 // P0, G[.][0], G[.][1], ...; the stage boundary loads the row of the code
 // just found straight into registers.  The distance of codeword k is
-// s * (-2 p.c_k) + ||c_k||^2 with s = 1 (plain metric) or 1 / max(||p||,
-// 1e-12) (cosine metric, codebook normalised in the tables); ties go to the
-// lowest index.  Every mbarrier wait is bounded.
+// -2 (s p).c_k + ||c_k||^2 with s = 1 (plain metric) or 1 / max(||p||, 1e-12)
+// (cosine metric, codebook normalised in the tables): the scale is applied to
+// the query before it is split, and the norms are added by a fourth MMA per
+// chunk -- A = [1 1 1 0 0 0 0 0] (or [0 0 0 0 1 1 1 0] for an odd chunk), a
+// constant in TMEM, times a block holding the three exact TF32 parts of each
+// ||c||^2 -- so the accumulator holds the distances themselves and the row
+// threads' scan is a minimum tree only.  Ties go to the lowest index.  Every
+// mbarrier wait is bounded.
 #include <atomic>
 
 #include "rvq_internal.cuh"
@@ -45,12 +51,12 @@ constexpr int S8_P = 3;                          // pipelines per CTA
 constexpr int S8_THREADS = 512;                  // warp 0 producer, 1-3 issuers, 4-15 rows
 constexpr uint32_t S8_TMEM_COLS = 512;
 constexpr uint32_t S8_PIPE_COLS = 160;
-constexpr uint32_t S8_A_HI = 0, S8_A_LO = 8, S8_ACC = 32;
+constexpr uint32_t S8_A_HI = 0, S8_A_LO = 8, S8_A_NORM = 16, S8_ACC = 32;  // A_NORM: even chunk, +8 odd
 constexpr uint32_t S8_IDESC = idesc_tf32(128, S8_KC);
 constexpr uint32_t S8_HALF = 128 * S8_D * 4;     // 4 KB: the hi or the lo block of a chunk
 constexpr int S8_TB = 4;                         // staging slots per pipeline
 constexpr uint32_t S8_STG_BYTES = S8_P * S8_TB * 2 * 128 * 16;  // [pipe][slot][half][frame] x 16 B
-constexpr uint32_t S8_XCH_BYTES = 2 * 2 * 128 * 4 * 2 + 2 * 128 * 4;  // values, indices, scales
+constexpr uint32_t S8_XCH_BYTES = 2 * 2 * 128 * 4 * 2;  // values, indices
 
 struct S8Bars {
   uint64_t img_full[2], img_free[2];
@@ -60,8 +66,9 @@ struct S8Bars {
   uint32_t pad;
 };
 
+constexpr uint32_t S8_NBLOCK = 128 * S8_D * 4;  // 4 KB: the norm operand of a pair of chunks
 __host__ __device__ constexpr uint32_t s8_buf_stride(int K) {
-  return ((uint32_t)K * (2 * S8_D * 4) + (uint32_t)K * 4 + 1023u) & ~1023u;
+  return ((uint32_t)K * (2 * S8_D * 4) + (uint32_t)cn_img8_blocks(K) * S8_NBLOCK + 1023u) & ~1023u;
 }
 __host__ __device__ constexpr size_t s8_smem_bytes(int K) {
   return 1024 + 2 * (size_t)s8_buf_stride(K) + S8_STG_BYTES + S8_XCH_BYTES + sizeof(S8Bars);
@@ -85,7 +92,7 @@ __device__ __forceinline__ float min64(const float (&v)[64]) {
 template <bool SPLIT>
 __global__ void __launch_bounds__(S8_THREADS, 1)
     k_search8_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
-                 const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
+                 const float *__restrict__ cn_img, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
                  int n_tiles, int metric, int *__restrict__ status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -94,14 +101,13 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
   constexpr int T = SPLIT ? 1 : S8_P;  // tiles per item
   const int nkc = K / S8_KC;
   const uint32_t img_bytes = (uint32_t)K * (2 * d * 4);
-  const uint32_t cn_bytes = (uint32_t)K * 4;
+  const uint32_t cn_bytes = (uint32_t)cn_img8_blocks(K) * S8_NBLOCK;
   const uint32_t buf_stride = s8_buf_stride(K);
   unsigned char *bufs = smem;
   unsigned char *stg = smem + 2 * buf_stride;
   float *xv = reinterpret_cast<float *>(stg + S8_STG_BYTES);  // [2][2][128]
   int *xk = reinterpret_cast<int *>(xv + 2 * 2 * 128);         // [2][2][128]
-  float *sbuf = reinterpret_cast<float *>(xk + 2 * 2 * 128);   // [2][128]
-  S8Bars &bar = *reinterpret_cast<S8Bars *>(sbuf + 2 * 128);
+  S8Bars &bar = *reinterpret_cast<S8Bars *>(xk + 2 * 2 * 128);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = (n_tiles + T - 1) / T;
   // one tile per CTA in the SPLIT variant
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
           unsigned char *dst = bufs + b * buf_stride;
           mbar_arrive_expect_tx(&bar.img_full[b], img_bytes + cn_bytes);
           bulk_g2s(dst, cb_img + (size_t)q * K * (2 * d), img_bytes, &bar.img_full[b]);
-          bulk_g2s(dst + img_bytes, cnorm + (size_t)q * K, cn_bytes, &bar.img_full[b]);
+          bulk_g2s(dst + img_bytes, cn_img + (size_t)q * (cn_bytes / 4), cn_bytes, &bar.img_full[b]);
         }
       // the copies still in flight land before the CTA may exit
       for (uint32_t gg = g > 2 ? g - 2 : 0; gg < g; ++gg) mbar_wait(&bar.img_full[gg & 1], (gg >> 1) & 1);
@@ -188,9 +194,12 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             const uint32_t chunk = buf0 + b * buf_stride + (uint32_t)c * (2 * S8_HALF);
             const uint64_t bhi = smem_desc(chunk, 16, 256, kSwizzle32B);
             const uint64_t blo = smem_desc(chunk + S8_HALF, 16, 256, kSwizzle32B);
+            const uint64_t bnorm = smem_desc(buf0 + b * buf_stride + img_bytes + (uint32_t)(c >> 1) * S8_NBLOCK, 16,
+                                             256, kSwizzle32B);
             mma_tf32_ta(acc, ta + S8_A_HI, blo, S8_IDESC, 0u);
             mma_tf32_ta(acc, ta + S8_A_HI, bhi, S8_IDESC, 1u);
             mma_tf32_ta(acc, ta + S8_A_LO, bhi, S8_IDESC, 1u);
+            mma_tf32_ta(acc, ta + S8_A_NORM + 8u * (uint32_t)(c & 1), bnorm, S8_IDESC, 1u);
             mma_commit(&bar.acc_full[p]);
             ++u;
           }
@@ -222,7 +231,14 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
     float part[d], gl[d];
 #pragma unroll
     for (int j = 0; j < d; ++j) part[j] = gl[j] = 0.0f;
-    float s_row = 1.0f;
+    {
+      // the norm MMA's A operands, constant: the even and the odd chunk's slots
+      const float a_even[d] = {1.f, 1.f, 1.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float a_odd[d] = {0.f, 0.f, 0.f, 0.f, 1.f, 1.f, 1.f, 0.f};
+      tmem_st8(lane_base + S8_A_NORM, a_even);
+      tmem_st8(lane_base + S8_A_NORM + 8, a_odd);
+      // (made visible by the tmem_wait_st before the first query's a_ready)
+    }
 
     // Term rows in flight: `npend` rows in staging slots 0.., the first one
     // added (the P0 row) when pend_p0, every other one subtracted.
@@ -281,23 +297,25 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             ss = fmaf(pq[j], pq[j], ss);
             part[j] = 0.0f;
           }
-          s_row = metric == RVQ_METRIC_COSINE ? 1.0f / fmaxf(sqrtf(ss), 1e-12f) : 1.0f;
+          if (metric == RVQ_METRIC_COSINE) {  // the query scaled by 1 / n(p) before the split
+            const float s_row = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+            for (int j = 0; j < d; ++j) pq[j] *= s_row;
+          }
           tmem_st8(lane_base + S8_A_HI, pq);  // raw = hi after TF32 truncation
 #pragma unroll
           for (int j = 0; j < d; ++j) pq[j] -= __uint_as_float(__float_as_uint(pq[j]) & 0xffffe000u);
           tmem_st8(lane_base + S8_A_LO, pq);
-          if (SPLIT) sbuf[b * 128 + f] = s_row;
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&bar.a_ready[p]);
         } else {
-          // pipelines 1, 2 of a split tile: this stage's query is built; its scale
+          // pipelines 1, 2 of a split tile: this stage's query is built
           if (!__all_sync(0xffffffffu, mbar_wait(&bar.a_ready[0], g & 1))) {
             record_error8(status, RVQ_DEVICE_TIMEOUT);
             ok = false;
             break;
           }
-          s_row = sbuf[b * 128 + f];
         }
         // ---- terms of the next query known before this stage's code:
         //      next stage: P0[n][q+1], G[q+1][0..q-1];  next item: P0[n'][0]
@@ -306,7 +324,6 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         const int64_t term_n = q + 1 < n_q ? n_row : n_next;
         int done = 0;
         // ---- scan this pipeline's chunks
-        const float *cn = reinterpret_cast<const float *>(bufs + b * buf_stride + img_bytes);
         float best_v = __int_as_float(0x7f800000);
         int best_k = 0;
         int i_own = 0;
@@ -317,11 +334,6 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             break;
           }
           ++ua;
-          if (i_own == 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.img_full[b], (g >> 1) & 1))) {
-            record_error8(status, RVQ_DEVICE_TIMEOUT);  // (the norms)
-            ok = false;
-            break;
-          }
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -333,14 +345,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
               tc_fence_before();
               mbar_arrive(&bar.acc_empty[p]);  // the accumulator is free: the values are in registers
             }
-            const float4 *cn4 = reinterpret_cast<const float4 *>(cn + c * S8_KC + 64 * h);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const float4 nv = cn4[u];
-              fma2(v[4 * u], v[4 * u + 1], s_row, nv.x, nv.y);
-              fma2(v[4 * u + 2], v[4 * u + 3], s_row, nv.z, nv.w);
-            }
-            const float m = min64(v);
+            const float m = min64(v);  // the distances themselves (norms added by the MMA)
             if (m <= best_v) {  // locate the first index holding m
               int first = 63;
 #pragma unroll
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
           }
         }
         if (!ok) break;
-        mbar_arrive(&bar.img_free[b]);  // this stage's norms have been read
+        mbar_arrive(&bar.img_free[b]);  // (kept in the count: every row thread is done with the stage)
         if (SPLIT) {
           // ---- pipelines 1, 2 hand their minima to pipeline 0
           const int xb = xu & 1;
@@ -463,7 +468,7 @@ cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *
   const size_t smem = s8_smem_bytes(dm.K);
   auto kern = split ? k_search8_tc<true> : k_search8_tc<false>;
   kern<<<grid, S8_THREADS, smem, st>>>(p0, at<float>(tables, L.g), at<float>(tables, L.cb_img),
-                                       at<float>(tables, L.cnorm), codes, n, n_q, dm.K, tiles, dm.metric, status);
+                                       at<float>(tables, L.cn_img8), codes, n, n_q, dm.K, tiles, dm.metric, status);
   return cudaGetLastError();
 }
 
