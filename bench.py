@@ -39,21 +39,19 @@ import rvq_inputs as ri  # noqa: E402
 WORKLOAD = "large_batch"
 METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) per frame of
-# one call, each with the sha256 (first 16 hex digits) of the kernel source it
-# was taken with: a figure whose source has changed since is reported as null.
-# Encode: a one-wave capture (38 912 frames; the traffic follows the frame
-# count); decode: a capture of the full workload (its DRAM counters take one
-# ncu pass).  The profile files hold the commands and the figures.
+# one call of the full workload (these counters take one ncu pass), each with
+# the sha256 (first 16 hex digits) of the sources it was taken with: a figure
+# whose sources have changed since is reported as null.  The profile files
+# hold the commands and the figures.
 TRAFFIC = {
     ("encode", "large_batch"): {
-        "bytes_per_frame": (167.62e6 + 42.57e6 + 91.36e6 + 0.58e6) / 38912,
-        "source": "residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu",
-        "sha16": "96d467b51046a69a",
+        "bytes_per_frame": (826.98e6 + 358.17e6 + 429.68e6 + 8.05e6) / 192000,
+        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu": "06cdf7acce6c9fbf",
+                    "residual_vector_quantisation_gb300/csrc/rvq_api.cu": "4f5bf68560f9671d"},
         "profile": "profiles/encode_tc_large_batch.md"},
     ("decode", "large_batch"): {
-        "bytes_per_frame": (52.42e6 + 738.95e6) / 192000,  # the full workload (one pass)
-        "source": "residual_vector_quantisation_gb300/csrc/rvq_decode.cu",
-        "sha16": "eaf30fea13b8b140",
+        "bytes_per_frame": (52.42e6 + 738.95e6) / 192000,
+        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_decode.cu": "eaf30fea13b8b140"},
         "profile": "profiles/decode_large_batch.md"},
 }
 L2_BYTES = 129 * 2 ** 20
@@ -80,7 +78,9 @@ def traffic_per_frame(op: str, workload: str):
     """DRAM bytes per frame from the committed capture, or None when there is
     none for this workload or the kernel source has changed since."""
     t = TRAFFIC.get((op, workload))
-    if not t or t["bytes_per_frame"] is None or source_sha16(t["source"]) != t["sha16"]:
+    if not t or t["bytes_per_frame"] is None:
+        return None
+    if any(source_sha16(path) != sha for path, sha in t["sources"].items()):
         return None
     return t["bytes_per_frame"]
 

@@ -177,7 +177,7 @@ RVQ_API rvq_status rvq_prepare(rvq_dims dims, const rvq_weights *weights, void *
  * are invalid (read it after the stream reaches the call).  The rest holds the
  * per-frame stage projections ([chunk][n_q*d] float32) of one chunk of
  * frames; encode works through the frames chunk by chunk.  This returns the
- * size for chunks of up to about 96 MiB of projections.  A larger scratch is
+ * size for chunks of up to about 512 MiB of projections.  A larger scratch is
  * accepted and used for larger chunks; a smaller one (at least
  * rvq_encode_min_scratch_bytes) gives smaller chunks. */
 RVQ_API size_t rvq_encode_scratch_bytes(rvq_dims dims, int64_t n_frames, int32_t n_q);

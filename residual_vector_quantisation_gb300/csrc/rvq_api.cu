@@ -13,7 +13,10 @@ namespace {
 
 using rvq::TablesLayout;
 
-constexpr size_t kChunkTargetBytes = size_t(96) << 20;  // projections per encode chunk
+// projections per encode chunk: large enough that a call of a few hundred
+// thousand frames runs in one chunk (one launch of each kernel: on 192 000
+// frames 1.544 ms against 1.601 ms in five chunks of 38 912)
+constexpr size_t kChunkTargetBytes = size_t(512) << 20;
 constexpr int64_t kChunkQuantum = 128;                   // frames
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

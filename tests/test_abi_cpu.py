@@ -68,7 +68,7 @@ def test_early_return_paths(lib_path):
     assert lib.rvq_tables_bytes(ok) > 8 * 1024 * 1024 * 4                # holds Z at least
     assert lib.rvq_encode_min_scratch_bytes(ok, 8) == 256 + 128 * 8 * 64 * 4
     assert lib.rvq_encode_scratch_bytes(ok, 100, 8) == 256 + 100 * 8 * 64 * 4
-    assert lib.rvq_encode_scratch_bytes(ok, 10 ** 6, 8) <= 256 + (96 << 20)
+    assert lib.rvq_encode_scratch_bytes(ok, 10 ** 6, 8) <= 256 + (512 << 20)
     assert lib.rvq_encode(ok, None, None, 5, 8, None, None, 0, None) == -1
     assert lib.rvq_encode(ok, None, None, 0, 8, None, None, 0, None) == 0
     assert lib.rvq_decode(ok, None, None, 5, 0, None, None, None) == -1
