@@ -34,9 +34,13 @@ namespace {
 // each output float is the sum of n_q table reads, and the gathers run at
 // about 22 TB/s of L2 reads on the GB300.
 
-// n_q, K and D/4 fixed at compile time (the OmniVoice codec's 8 x 1024 x 1024
-// shape): the compiler then keeps all n_q row loads of a thread in flight,
-// about 1.5x faster than the general kernel below.
+// n_q, K and D/4 fixed at compile time: the compiler then keeps the row
+// loads of a thread in flight, about 1.4x faster than the general kernel
+// below on the OmniVoice codec's 8 x 1024 x 1024 shape.  Instantiated for the
+// shapes of the codecs on the source pages (OmniVoice: 8 stages of 1024
+// entries into 1024; MOSS: 32 stages into 768, 9-10 % faster than the general
+// kernel; Audio8: 10 stages of 4096, 21 % faster).  (OmniVoice with fc2, 256
+// wide, measured the same either way and takes the general kernel.)
 template <int NQ, int KC, int DC>
 __global__ void __launch_bounds__(DC) k_decode_fixed(const float4 *__restrict__ Z4, const float4 *__restrict__ b4,
                                                      const int *__restrict__ b_used, const int32_t *__restrict__ codes,
@@ -124,8 +128,16 @@ cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t 
   float4 *y4 = reinterpret_cast<float4 *>(y);
   if (n > 0x7fffffffLL) return cudaErrorInvalidValue;  // one CTA per frame
   const dim3 grid((unsigned)n);
-  if (n_q == 8 && dm.K == 1024 && D4 == 256) {
+  if (dm.K == 1024 && n_q == 8 && D4 == 256) {
     k_decode_fixed<8, 1024, 256><<<grid, 256, 0, st>>>(Z4, b4, b_used, codes, y4, bad_u);
+    return cudaGetLastError();
+  }
+  if (dm.K == 1024 && n_q == 32 && D4 == 192) {
+    k_decode_fixed<32, 1024, 192><<<grid, 192, 0, st>>>(Z4, b4, b_used, codes, y4, bad_u);
+    return cudaGetLastError();
+  }
+  if (dm.K == 4096 && n_q == 10 && D4 == 256) {
+    k_decode_fixed<10, 4096, 256><<<grid, 256, 0, st>>>(Z4, b4, b_used, codes, y4, bad_u);
     return cudaGetLastError();
   }
   const int threads = D4 >= 256 ? 256 : (D4 + 31) / 32 * 32;
