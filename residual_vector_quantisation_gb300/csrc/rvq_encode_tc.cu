@@ -293,7 +293,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // area, subtracted from the partial sum one chunk later (the P0 row is copied
 // straight into the partial); the stage boundary loads only the one row of
 // the code just found, straight into registers, and forms the query there.
-// Terms are added in the order s = 0, 1, ..., q.
+// Terms are added in the order s = 0, 1, ..., q.  A launch over a block of
+// stages [q_begin, q_end) of a deep stack finds the terms of the earlier
+// blocks already subtracted from P0 (k_cross_terms) and sums from q_begin.
 // A launch with no more tiles than SMs (the SPLIT variant, for a stage of an
 // even number of chunks) gives each CTA one tile and splits it: both
 // pipelines work on that tile, pipeline t taking the chunks c = t mod 2, so
@@ -357,8 +359,8 @@ static_assert(SR_SMEM <= 227 * 1024, "search kernel shared memory");
 template <int MODE, bool SHARE = false>
 __global__ void __launch_bounds__(SR_THREADS, 1)
     k_search_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
-                const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
-                int n_tiles, int metric, int *__restrict__ status) {
+                const float *__restrict__ cnorm, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int q_begin,
+                int q_end, int K, int n_tiles, int metric, int *__restrict__ status) {
   constexpr bool SPLIT = MODE >= 1, CPAIR = MODE == 2;
   // this CTA's item index and the number of such (a CTA pair counts once);
   // unsigned, like blockIdx.x itself (signed forms measured 2.5 % slower:
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       uint32_t ch = 0;  // chunks gone through
       bool ok = true;
       for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep)
-        for (int q = 0; q < n_q && ok; ++q)
+        for (int q = q_begin; q < q_end && ok; ++q)
           for (int c = (int)prank; c < nkc && ok; c += C_STEP, ++ch) {
             const int cr = (c + rot) % nkc;
             if (role == 2) {
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
         if (t == 1 && !pair && !SPLIT) break;
         const bool turns = SPLIT || pair;
         const bool twice = !pair;  // sole user of each half-chunk
-        for (int q = 0; q < n_q && ok; ++q, ++builds)
+        for (int q = q_begin; q < q_end && ok; ++q, ++builds)
           for (int c = (int)prank; c < nkc && ok; c += C_STEP, ++ch) {
             if (SPLIT && ((CPAIR ? c >> 1 : c) & 1) != t) continue;
             const uint32_t j0 = 2 * ch, j1 = j0 + 1;  // the chunk's lo and hi half-chunks
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     // the first query's partial: the projection row itself (tile 1 only if the first item has one)
     if (tile == 0 || (!SPLIT && CTA_ID + n_cta < n_tiles)) {
       const int64_t n = (int64_t)(CTA_ID + tile * n_cta) * 128 + quarter * 32 + lane;
-      term_issue(P0 + (n < n_rows ? n : 0) * ld, true);
+      term_issue(P0 + (n < n_rows ? n : 0) * ld + q_begin * d, true);
     }
     uint32_t xs = 0;  // CTA pairs: stage minima exchanged
     for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep) {
@@ -640,7 +642,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       const bool alone = !pair && !split;
       const int n_own = CPAIR ? nkc / 4 : split ? nkc / 2 : nkc;  // chunks scanned per stage
       constexpr bool share_terms = SPLIT && SHARE;
-      for (int q = 0; q < n_q && ok; ++q) {
+      for (int q = q_begin; q < q_end && ok; ++q) {
         if (!scan_only) {
           // ---- stage boundary: the query = partial - the last known term (if
           //      still staged) - the row of the code just found (zero at the
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           //      no shared memory.  (Subtracting the zero row is exact, and
           //      keeps one code path.)
           float4 g[d / 4];
-          const bool has_g = q > 0;
+          const bool has_g = q > q_begin;
 #pragma unroll
           for (int u = 0; u < d / 4; ++u) g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (has_g) {
@@ -668,7 +670,8 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           __syncwarp();  // the warp's copies (this frame's staged row among them) have landed
           // split items: pipeline 1's partial of this query's terms (q - (q + 1) / 2
           // of the q fetched during the last stage), in this frame's TMEM lane
-          const bool sub_p1 = share_terms && q > 0 && q - (q + 1) / 2 > 0;
+          const int q_rel = q - q_begin;
+          const bool sub_p1 = share_terms && q_rel > 0 && q_rel - (q_rel + 1) / 2 > 0;
           if (sub_p1) {
             if (!__all_sync(0xffffffffu, mbar_wait(&bar.p1t_full, p1u & 1))) {
               record_error(status, RVQ_DEVICE_TIMEOUT);
@@ -721,7 +724,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           // scaled by 1 / max(||p||, 1e-12) in the scan
           s_row = metric == RVQ_METRIC_COSINE ? 1.0f / fmaxf(sqrtf(ss), 1e-12f) : 1.0f;
           // for pipeline 1: the distance scale, and the code just found (its terms need it)
-          if (split) tmem_st2(xch + 4, __float_as_uint(s_row), share_terms && q > 0 ? (uint32_t)my_codes[q - 1] : 0u);
+          if (split) tmem_st2(xch + 4, __float_as_uint(s_row), share_terms && q > q_begin ? (uint32_t)my_codes[q - 1] : 0u);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(a_ready);
@@ -739,23 +742,23 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           tmem_ld2(xch + 4, sv, code_prev);
           tmem_wait_ld();
           s_row = __uint_as_float(sv);
-          if (share_terms && q > 0) my_codes[q - 1] = (int)code_prev;
+          if (share_terms && q > q_begin) my_codes[q - 1] = (int)code_prev;
         }
         // ---- terms of the next query known before this stage's code:
-        //      next stage: P0[n][q+1], G[q+1][0..q-1];  next tile: P0[n'][0]
-        const int q_next = q + 1 < n_q ? q + 1 : 0;
-        const int n_terms_all = q + 1 < n_q ? q + 1 : (has_next ? 1 : 0);
+        //      next stage: P0[n][q+1], G[q+1][q_begin..q-1];  next tile: P0[n'][q_begin]
+        const int q_next = q + 1 < q_end ? q + 1 : q_begin;
+        const int n_terms_all = q + 1 < q_end ? q + 1 - q_begin : (has_next ? 1 : 0);
         // split items of deep stacks: pipeline 0 fetches the first half of the
         // terms (P0 first) into its partial in shared memory, pipeline 1 the
         // rest into a partial of its own in TMEM, subtracted at the stage
         // boundary, so each has half the fetch round trips
         const int n_half = share_terms ? (n_terms_all + 1) / 2 : n_terms_all;
         const int n_terms = scan_only ? 0 : n_half;
-        const int n_p1 = share_terms && q + 1 < n_q ? n_terms_all - n_half : 0;
-        const int64_t n_row = q + 1 < n_q ? (valid ? n : 0) : (n_next < n_rows ? n_next : 0);
+        const int n_p1 = share_terms && q + 1 < q_end ? n_terms_all - n_half : 0;
+        const int64_t n_row = q + 1 < q_end ? (valid ? n : 0) : (n_next < n_rows ? n_next : 0);
         auto term_row = [&](int t) -> const float * {
           return t == 0 ? P0 + n_row * ld + q_next * d
-                        : G + ((size_t)pair_index(q_next, t - 1) * K + my_codes[t - 1]) * d;
+                        : G + ((size_t)pair_index(q_next, q_begin + t - 1) * K + my_codes[q_begin + t - 1]) * d;
         };
         int done = 0, done1 = 0;
         // ---- scan the K distances ||c||^2 - 2 p.c; keep the lexicographic (value, index) minimum
@@ -937,6 +940,61 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
 }
 
 // ===========================================================================
+// Stage blocks of deep stacks.  The query of stage t is
+//   p_t = P0[n][t] - sum_{s<t} G[t][s][code_s],
+// t terms of which a search launch over all stages would gather t - 1 (one
+// 256-byte row each) between the distance chunks of stage t - 1: 496 rows a
+// frame at 32 stages, with one or two in flight per row thread.  A deep stack
+// therefore runs as a few search launches over blocks of stages [q_begin,
+// q_end), each gathering only the terms of its own block (s >= q_begin); the
+// terms of the earlier stages are all known once the previous blocks are
+// done, and this kernel subtracts them from P0[n][q_begin..q_end) first, with
+// many rows in flight on every SM.  The order is the search kernel's own:
+// s = 0, 1, ..., q_begin - 1 here, then q_begin, ... in the search.
+// One half-warp per (frame, stage t), one float4 column per lane; a code
+// outside [0, K) (an earlier launch that gave up) reads row 0.
+// ===========================================================================
+constexpr int CT_THREADS = 256;
+constexpr int CT_UNROLL = 8;
+
+__global__ void __launch_bounds__(CT_THREADS)
+    k_cross_terms(float *__restrict__ P0, const float *__restrict__ G, const int32_t *__restrict__ codes,
+                  int64_t n_rows, int n_q, int q_begin, int q_end, int K) {
+  constexpr int d = kCodeDim;
+  const int nt = q_end - q_begin;
+  const int64_t item = ((int64_t)blockIdx.x * CT_THREADS + threadIdx.x) >> 4;
+  if (item >= n_rows * nt) return;
+  const int l = threadIdx.x & 15;
+  const int64_t n = item / nt;
+  const int t = q_begin + (int)(item - n * nt);
+  const int32_t *cr = codes + n * n_q;
+  float4 *dst = reinterpret_cast<float4 *>(P0 + (n * n_q + t) * d) + l;
+  const float4 *g = reinterpret_cast<const float4 *>(G + (size_t)pair_index(t, 0) * K * d) + l;
+  float4 acc = *dst;
+  for (int s0 = 0; s0 < q_begin; s0 += CT_UNROLL) {
+    int c[CT_UNROLL];
+#pragma unroll
+    for (int u = 0; u < CT_UNROLL; ++u) {
+      const int v = s0 + u < q_begin ? __ldg(cr + s0 + u) : 0;
+      c[u] = (unsigned)v < (unsigned)K ? v : 0;
+    }
+    float4 r[CT_UNROLL];
+#pragma unroll
+    for (int u = 0; u < CT_UNROLL; ++u)
+      if (s0 + u < q_begin) r[u] = __ldg(g + ((size_t)(s0 + u) * K + c[u]) * (d / 4));
+#pragma unroll
+    for (int u = 0; u < CT_UNROLL; ++u)
+      if (s0 + u < q_begin) {
+        acc.x -= r[u].x;
+        acc.y -= r[u].y;
+        acc.z -= r[u].z;
+        acc.w -= r[u].w;
+      }
+  }
+  *dst = acc;
+}
+
+// ===========================================================================
 // host side
 // ===========================================================================
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
@@ -1024,11 +1082,20 @@ int max_search_clusters() {
 // Measured: 32 stages 15 % faster; 8 and 10 stages 5 % slower.
 bool share_terms(int n_q, int own_chunks) { return n_q > 2 * own_chunks; }
 
-// One tile per cluster of CS CTAs.
+// Stage blocks of a call (k_cross_terms): a stack deeper than kStageBlock
+// whose row threads would fetch more than two terms a chunk at its last
+// stage runs in the fewest blocks of at most kStageBlock stages (sizes as
+// equal as they go).
+constexpr int kStageBlock = 8;
+int stage_blocks(int n_q, int own_chunks) {
+  return n_q > kStageBlock && n_q > 2 * own_chunks ? (n_q + kStageBlock - 1) / kStageBlock : 1;
+}
+
+// One tile per cluster of CS CTAs, stages [q0, q1).
 template <int CS>
 cudaError_t launch_search_clusters(const float *p0, const float *G, const float *cb_img, const float *cn,
-                                   int32_t *codes, int64_t n, int n_q, int K, int tiles, int metric, int *status,
-                                   cudaStream_t st) {
+                                   int32_t *codes, int64_t n, int n_q, int q0, int q1, int K, int tiles, int metric,
+                                   int *status, cudaStream_t st) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(CS * tiles), 1, 1);
   cfg.blockDim = dim3(SR_THREADS, 1, 1);
@@ -1041,8 +1108,8 @@ cudaError_t launch_search_clusters(const float *p0, const float *G, const float 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kern = share_terms(n_q, K / SR_KC / 4) ? k_search_tc<CS, true> : k_search_tc<CS, false>;
-  return cudaLaunchKernelEx(&cfg, kern, p0, G, cb_img, cn, codes, n, n_q, K, tiles, metric, status);
+  auto kern = share_terms(q1 - q0, K / SR_KC / 4) ? k_search_tc<CS, true> : k_search_tc<CS, false>;
+  return cudaLaunchKernelEx(&cfg, kern, p0, G, cb_img, cn, codes, n, n_q, q0, q1, K, tiles, metric, status);
 }
 
 int sm_count() {
@@ -1133,16 +1200,32 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   const int nkc = K / SR_KC;
   const float *G = at<float>(tables, L.g), *cb_img = at<float>(tables, L.cb_img), *cn = at<float>(tables, L.cnorm);
   int32_t *codes_c = codes + n0 * n_q;
-  // one wave of CTA pairs: each tile's chunks split over two SMs
-  if (nkc % 4 == 0 && tiles <= max_search_clusters<2>())
-    return launch_search_clusters<2>(p0, G, cb_img, cn, codes_c, n, n_q, K, tiles, dm.metric, status, st);
-  // no more tiles than SMs: every item is split, and the ring takes tile 1's areas
-  auto search = tiles <= sms && nkc % 2 == 0
-                    ? (share_terms(n_q, nkc / 2) ? k_search_tc<1, true> : k_search_tc<1, false>)
-                    : k_search_tc<0>;
-  search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, G, cb_img, cn, codes_c, n, n_q, K, tiles,
-                                                                 dm.metric, status);
-  return cudaGetLastError();
+  // one wave of CTA pairs: each tile's chunks split over two SMs; else, with
+  // no more tiles than SMs, every item is split and the ring takes tile 1's areas
+  const bool pairs = nkc % 4 == 0 && tiles <= max_search_clusters<2>();
+  const bool split = !pairs && tiles <= sms && nkc % 2 == 0;
+  const int own = pairs ? nkc / 4 : split ? nkc / 2 : nkc;  // chunks a pipeline scans per stage
+  const int nb = stage_blocks(n_q, own);
+  for (int b = 0; b < nb; ++b) {
+    const int q0 = (int)((int64_t)n_q * b / nb), q1 = (int)((int64_t)n_q * (b + 1) / nb);
+    if (q0 > 0) {
+      const int64_t threads = n * (q1 - q0) * 16;
+      k_cross_terms<<<(unsigned)((threads + CT_THREADS - 1) / CT_THREADS), CT_THREADS, 0, st>>>(p0, G, codes_c, n,
+                                                                                               n_q, q0, q1, K);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (pairs) {
+      e = launch_search_clusters<2>(p0, G, cb_img, cn, codes_c, n, n_q, q0, q1, K, tiles, dm.metric, status, st);
+    } else {
+      auto search = split ? (share_terms(q1 - q0, nkc / 2) ? k_search_tc<1, true> : k_search_tc<1, false>)
+                          : k_search_tc<0>;
+      search<<<tiles < sms ? tiles : sms, SR_THREADS, SR_SMEM, st>>>(p0, G, cb_img, cn, codes_c, n, n_q, q0, q1, K,
+                                                                     tiles, dm.metric, status);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace rvq

@@ -226,6 +226,24 @@ def test_tiles_on_clusters(K, Q, N, metric):
         rq.rvq_set_stream_max_frames(prev)
 
 
+@pytest.mark.parametrize("K,Q,N,metric", [(512, 20, 3000, "l2"), (768, 20, 3000, "l2"), (768, 13, 2000, "cosine"),
+                                          (1024, 17, 155 * 128 - 40, "l2")])
+def test_deep_stacks_in_stage_blocks(K, Q, N, metric):
+    """Stacks deeper than eight stages whose terms outnumber a pipeline's
+    chunks run as several search launches over blocks of stages, the terms of
+    earlier blocks subtracted from the projections in between: on CTA pairs
+    (K = 512), split items (K = 768) and two-tile items (155 tiles, more than
+    the SMs), with ragged blocks (20 = 6 + 7 + 7, 13 = 6 + 7, 17 = 5 + 6 + 6).
+    The tile kernels are forced; every frame is checked."""
+    prev = rq.rvq_set_stream_max_frames(0)
+    try:
+        w, W = _small_weights(D=64, K=K, Q=Q, seed=K + Q, bias=True, decay=0.9)
+        x = np.random.default_rng(K + N).standard_normal((N, 64)).astype(np.float32)
+        run_small(W, x, label=f"K={K} Q={Q} N={N} {metric}", metric=metric)
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
+
+
 def test_biases_and_prefix_depths():
     w, W = _small_weights(D=256, K=512, Q=6, bias=True)
     x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
