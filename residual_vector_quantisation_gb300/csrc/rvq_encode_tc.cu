@@ -645,29 +645,47 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       for (int q = q_begin; q < q_end && ok; ++q) {
         if (!scan_only) {
           // ---- stage boundary: the query = partial - the last known term (if
-          //      still staged) - the row of the code just found (zero at the
-          //      first stage).  This frame's row of the latter is loaded straight
-          //      into registers (first, so its latency overlaps the wait for the
-          //      staged term), and the query is formed in registers: the
-          //      boundary reads the partial and the staged row once and writes
-          //      no shared memory.  (Subtracting the zero row is exact, and
-          //      keeps one code path.)
-          float4 g[d / 4];
-          const bool has_g = q > q_begin;
-#pragma unroll
-          for (int u = 0; u < d / 4; ++u) g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (has_g) {
-            const float4 *gr =
-                reinterpret_cast<const float4 *>(G + ((size_t)pair_index(q, q - 1) * K + my_codes[q - 1]) * d);
-#pragma unroll
-            for (int u = 0; u < d / 4; ++u) g[u] = __ldg(gr + u);
-          }
+          //      still staged) - the row of the code just found (none at the
+          //      block's first stage).  The partial minus the staged term is read
+          //      into registers; the staging area then takes the rows of the codes
+          //      just found, copied cooperatively like every term (a row per
+          //      thread would take one L1 wavefront per lane and load), and the
+          //      query is formed in registers: the boundary writes no shared
+          //      memory.
           const bool sub_staged = pending && !pending_first;
           if (pending) {
             cp_async_wait_all();
             pending = false;
           }
           __syncwarp();  // the warp's copies (this frame's staged row among them) have landed
+          float4 pq[d / 4];
+#pragma unroll
+          for (int u = 0; u < d / 4; ++u) {
+            const int idx = lane * (d / 4) + (u ^ (lane & 7));
+            pq[u] = wpart[idx];
+            if (sub_staged) {
+              const float4 v = wstage[idx];
+              pq[u].x -= v.x;
+              pq[u].y -= v.y;
+              pq[u].z -= v.z;
+              pq[u].w -= v.w;
+            }
+          }
+          if (q > q_begin) {
+            __syncwarp();  // every lane has read its staged row before the code rows overwrite it
+            term_issue(G + ((size_t)pair_index(q, q - 1) * K + my_codes[q - 1]) * d, false);
+            cp_async_wait_all();
+            pending = false;
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < d / 4; ++u) {
+              const float4 v = wstage[lane * (d / 4) + (u ^ (lane & 7))];
+              pq[u].x -= v.x;
+              pq[u].y -= v.y;
+              pq[u].z -= v.z;
+              pq[u].w -= v.w;
+            }
+          }
           // split items: pipeline 1's partial of this query's terms (q - (q + 1) / 2
           // of the q fetched during the last stage), in this frame's TMEM lane
           const int q_rel = q - q_begin;
@@ -688,19 +706,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             float p[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const int idx = lane * (d / 4) + ((8 * h + u) ^ (lane & 7));
-              float4 t = wpart[idx];
-              if (sub_staged) {
-                const float4 v = wstage[idx];
-                t.x -= v.x;
-                t.y -= v.y;
-                t.z -= v.z;
-                t.w -= v.w;
-              }
-              t.x -= g[8 * h + u].x;
-              t.y -= g[8 * h + u].y;
-              t.z -= g[8 * h + u].z;
-              t.w -= g[8 * h + u].w;
+              const float4 t = pq[8 * h + u];
               p[4 * u] = t.x;
               p[4 * u + 1] = t.y;
               p[4 * u + 2] = t.z;
@@ -809,11 +815,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
           mbar_arrive(&bar.cn_free[sn]);  // the norms are in registers
           if (alone) mbar_arrive(&bar.cn_free[sn]);
           if (m <= best_v) {  // rare after the first chunks: locate the first index holding m
-            int first = SR_KC - 1;
-#pragma unroll
-            for (int i = SR_KC - 1; i >= 0; --i)
-              if (v[i] == m) first = i;
-            const int k = cr * SR_KC + first;
+            const int k = cr * SR_KC + first_index_of(v, m);
             if (m < best_v || k < best_k) {
               best_v = m;
               best_k = k;

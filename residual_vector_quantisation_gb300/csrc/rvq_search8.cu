@@ -347,11 +347,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             }
             const float m = min64(v);  // the distances themselves (norms added by the MMA)
             if (m <= best_v) {  // locate the first index holding m
-              int first = 63;
-#pragma unroll
-              for (int i = 63; i >= 0; --i)
-                if (v[i] == m) first = i;
-              const int k = c * S8_KC + 64 * h + first;
+              const int k = c * S8_KC + 64 * h + first_index_of(v, m);
               if (m < best_v || k < best_k) {
                 best_v = m;
                 best_k = k;

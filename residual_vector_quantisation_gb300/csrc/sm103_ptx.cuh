@@ -416,6 +416,29 @@ __device__ __forceinline__ float min128(const float (&v)[128]) {
   return fminf(fmin3(c[0], c[1], c[2]), fminf(c[3], c[4]));
 }
 
+// The lowest i with v[i] == m (N - 1 if there is none): eight independent
+// searches over N/8 values each, combined by min, so that no select waits on
+// the N - 1 before it (one chain over all N values took longer than the
+// distance arithmetic of the chunk).
+template <int N>
+__device__ __forceinline__ int first_index_of(const float (&v)[N], float m) {
+  constexpr int R = 8, L = N / R;
+  static_assert(N % R == 0, "eight equal ranges");
+  int f[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    f[r] = N - 1;
+#pragma unroll
+    for (int i = L - 1; i >= 0; --i)
+      if (v[L * r + i] == m) f[r] = L * r + i;
+  }
+#pragma unroll
+  for (int w = 1; w < R; w *= 2)
+#pragma unroll
+    for (int r = 0; r + w < R; r += 2 * w) f[r] = min(f[r], f[r + w]);
+  return f[0];
+}
+
 // ---------------------------------------------------------------------------
 // descriptors
 // ---------------------------------------------------------------------------
