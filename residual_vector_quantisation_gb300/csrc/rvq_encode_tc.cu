@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
     // tile, each does its waits while the other tile's MMAs are queued.  The
     // two take turns chunk by chunk (tile 0, tile 1, tile 0, ...; in a split
     // item, the even and the odd chunks): an issuer hands over the turn after
-    // 20 of its 24 MMAs, so the next chunk's MMAs queue up behind the last
+    // 18 of its 24 MMAs, so the next chunk's MMAs queue up behind the last
     // ones without a gap, and the pipeline that has just finished scans its
     // distances while the tensor core works on the other.  The 24 MMAs of a
     // chunk are issued straight-line (compile-time operand offsets and
@@ -502,6 +502,13 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
       bool ok = true;
       auto wait_or_fail = [&](uint64_t *b, uint32_t parity) {
         if (ok && !mbar_wait(b, parity)) {
+          record_error(status, RVQ_DEVICE_TIMEOUT);
+          ok = false;
+        }
+        return ok;
+      };
+      auto wait_hot_or_fail = [&](uint64_t *b, uint32_t parity) {
+        if (ok && !mbar_wait_hot(b, parity)) {
           record_error(status, RVQ_DEVICE_TIMEOUT);
           ok = false;
         }
@@ -526,7 +533,8 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             if (u > 0 && !wait_or_fail(&bar.acc_empty[t], (u - 1) & 1)) break;
             if (c == (CPAIR ? (int)prank + 2 * t : SPLIT ? t : 0) && !wait_or_fail(&bar.a_ready[SPLIT ? 0 : t], builds & 1)) break;
             if (!wait_or_fail(&bar.b_full[s0], (j0 / SLOTS) & 1)) break;
-            if (turns && (t == 1 || u > 0) && !wait_or_fail(&bar.turn[t], (t == 1 ? u : u - 1) & 1)) break;
+            // (the turn is polled: its wait is the one the tensor core idles on)
+            if (turns && (t == 1 || u > 0) && !wait_hot_or_fail(&bar.turn[t], (t == 1 ? u : u - 1) & 1)) break;
             ++u;
             tc_fence_after();
             // lo half first (a_hi.b_lo, 8 MMAs), then hi (a_hi.b_hi + a_lo.b_hi, 16): the
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
             const uint64_t bd_hi = desc0 + (uint64_t)((s1 * SR_HALF) >> 4);
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-              if (m == 6) mbar_arrive(&bar.turn[1 - t]);  // 20 of 24 issued: hand over
+              if (m == 5) mbar_arrive(&bar.turn[1 - t]);  // 18 of 24 issued: hand over
               const uint64_t b = bd_hi + (uint64_t)((((m >> 2) * SR_ATOM) + (m & 3) * 32) >> 4);
               mma_tf32_ta(tb + SR_ACC, ta + SR_A_HI + (uint32_t)m * 8, b, SR_IDESC, 1u);
               mma_tf32_ta(tb + SR_ACC, ta + SR_A_LO + (uint32_t)m * 8, b, SR_IDESC, 1u);
