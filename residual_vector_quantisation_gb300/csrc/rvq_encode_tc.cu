@@ -273,8 +273,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // one tile per copy).  The two tiles' MMA issuers take turns chunk by chunk,
 // so the tensor core works on one tile's chunk while the other tile scans its
 // distances.
-//   * a ring of three (split: five) half-chunks, one 32 KB bulk copy each (a bulk copy takes
-//     about the same time whatever its size, so copies are large): a chunk is
+//   * a ring of three (split: five) 32 KB half-chunks, each brought in by two
+//     16 KB bulk copies from two threads (a thread's copies run one after
+//     another, each in about the same time whatever its size): a chunk is
 //     128 codewords of -2*c as four atoms of 128 rows x 128 B, pre-swizzled --
 //     hi dims 0-31, hi 32-63 (hi half), lo 0-31, lo 32-63 (lo half); the lo
 //     half is copied and used first;
@@ -315,7 +316,8 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // ===========================================================================
 constexpr int SR_KC = 128;                    // codewords per chunk (MMA N)
 constexpr uint32_t SR_ATOM = 128 * 128;       // 128 codewords x 128 B
-constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // one bulk copy: hi or lo part of a chunk
+constexpr uint32_t SR_HALF = 2 * SR_ATOM;     // hi or lo part of a chunk
+constexpr int SR_COPY_PIECES = 2;             // bulk copies (and producer threads) per half-chunk
 constexpr int SR_SLOTS = 3;                   // half-chunks in the ring
 constexpr int SR_SLOTS_SPLIT = 5;             // ... when every item is split: plus tile 1's two areas
 constexpr int SR_SLOTS_CPAIR = 4;             // ... split across a CTA pair: tile 1's staging area holds the pair's minima
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
 
   if (tid == 0) {
     for (int s = 0; s < SLOTS; ++s) {
-      mbar_init(&bar.b_full[s], 1);
+      mbar_init(&bar.b_full[s], SR_COPY_PIECES);
       mbar_init(&bar.b_empty[s], 2);  // one commit per tile's MMA issuer
     }
     for (int s = 0; s < SR_CN_SLOTS; ++s) {
@@ -431,14 +433,18 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
   const uint32_t tmem = bar.tmem;
 
   if (warp == 0 || warp == 11) {
-    // ---------------- producers: warp 0 lane 0 the lo halves, lane 1 the norms; warp 11 the hi halves ----------------
+    // ---------------- producers: warp 0 lanes 0-1 the lo halves, lane 2 the norms; warp 11 lanes 0-1 the hi halves ----------------
     // A thread's bulk copies are carried out one after another (about a third
     // of a microsecond each, whatever their size), so each kind of copy gets
-    // a thread of its own: with one tile per CTA the tensor core needs a chunk
-    // every 0.8 us, about the time of two copies in a row.
-    const int role = warp == 11 ? 0 : (lane == 0 ? 1 : 2);  // 0: hi halves, 1: lo halves, 2: norms
-    const int h = role == 0 ? 0 : 1;                         // the half of a chunk image (hi, lo)
-    if (lane == 0 || (warp == 0 && lane == 1)) {
+    // threads of its own, each half-chunk copied in SR_COPY_PIECES pieces by
+    // as many threads: with one tile per CTA the tensor core needs a chunk
+    // every 0.8 us, about the time of two copies in a row (two pieces: mid-size
+    // encodes 1-2 % faster than whole halves, four: no better).
+    const int role = warp == 11 ? (lane < SR_COPY_PIECES ? 0 : -1)
+                                : (lane < SR_COPY_PIECES ? 1 : lane == SR_COPY_PIECES ? 2 : -1);  // hi, lo, norms
+    const int piece = lane;                                                // of a half-chunk
+    const int h = role == 0 ? 0 : 1;  // the half of a chunk image (hi, lo)
+    if (role >= 0) {
       uint32_t ch = 0;  // chunks gone through
       bool ok = true;
       for (int t0 = CTA_ID; t0 < n_tiles && ok; t0 += sweep)
@@ -465,9 +471,10 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&bar.b_full[s], SR_HALF);
-            bulk_g2s(ring + s * SR_HALF, cb_img + (((size_t)q * nkc + cr) * 2 + h) * (SR_HALF / 4), SR_HALF,
-                     &bar.b_full[s]);
+            constexpr uint32_t PB = SR_HALF / SR_COPY_PIECES;
+            mbar_arrive_expect_tx(&bar.b_full[s], PB);
+            bulk_g2s(ring + s * SR_HALF + piece * PB,
+                     cb_img + (((size_t)q * nkc + cr) * 2 + h) * (SR_HALF / 4) + piece * (PB / 4), PB, &bar.b_full[s]);
           }
       // Every copy is waited for by the threads that use it before the final
       // barrier; after an error, the last copy of this thread (whose slot no
@@ -961,20 +968,21 @@ __global__ void __launch_bounds__(SR_THREADS, 1)
 // done, and this kernel subtracts them from P0[n][q_begin..q_end) first, with
 // many rows in flight on every SM.  The order is the search kernel's own:
 // s = 0, 1, ..., q_begin - 1 here, then q_begin, ... in the search.
-// One half-warp per (frame, stage t), one float4 column per lane; a code
-// outside [0, K) (an earlier launch that gave up) reads row 0.
+// d/4 lanes per (frame, stage t), one float4 column each (d = 64 or 8); a
+// code outside [0, K) (an earlier launch that gave up) reads row 0.
 // ===========================================================================
 constexpr int CT_THREADS = 256;
 constexpr int CT_UNROLL = 8;
 
+template <int d>
 __global__ void __launch_bounds__(CT_THREADS)
     k_cross_terms(float *__restrict__ P0, const float *__restrict__ G, const int32_t *__restrict__ codes,
                   int64_t n_rows, int n_q, int q_begin, int q_end, int K) {
-  constexpr int d = kCodeDim;
+  constexpr int LPI = d / 4;  // lanes per item
   const int nt = q_end - q_begin;
-  const int64_t item = ((int64_t)blockIdx.x * CT_THREADS + threadIdx.x) >> 4;
+  const int64_t item = ((int64_t)blockIdx.x * CT_THREADS + threadIdx.x) / LPI;
   if (item >= n_rows * nt) return;
-  const int l = threadIdx.x & 15;
+  const int l = threadIdx.x % LPI;
   const int64_t n = item / nt;
   const int t = q_begin + (int)(item - n * nt);
   const int32_t *cr = codes + n * n_q;
@@ -1096,7 +1104,7 @@ bool share_terms(int n_q, int own_chunks) { return n_q > 2 * own_chunks; }
 // whose row threads would fetch more than two terms a chunk at its last
 // stage runs in the fewest blocks of at most kStageBlock stages (sizes as
 // equal as they go).
-constexpr int kStageBlock = 8;
+constexpr int kStageBlock = 6;
 int stage_blocks(int n_q, int own_chunks) {
   return n_q > kStageBlock && n_q > 2 * own_chunks ? (n_q + kStageBlock - 1) / kStageBlock : 1;
 }
@@ -1204,12 +1212,30 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   cudaError_t e = launch_project_tc(dm, tables, x + n0 * dim_in(dm), n, n_q, p0, status, false, st, -1);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
-  if (d == kCodeDimSmall)
-    return launch_search8(dm, tables, p0, n, n_q, codes + n0 * n_q, status, sms, st);
-  const int tiles = (int)((n + 127) / 128);
-  const int nkc = K / SR_KC;
   const float *G = at<float>(tables, L.g), *cb_img = at<float>(tables, L.cb_img), *cn = at<float>(tables, L.cnorm);
   int32_t *codes_c = codes + n0 * n_q;
+  // the terms of stages [0, q0) subtracted from P0[.][q0, q1)
+  auto cross_terms = [&](int q0, int q1) {
+    const int64_t threads = n * (q1 - q0) * (d / 4);
+    const unsigned blocks = (unsigned)((threads + CT_THREADS - 1) / CT_THREADS);
+    if (d == kCodeDimSmall)
+      k_cross_terms<kCodeDimSmall><<<blocks, CT_THREADS, 0, st>>>(p0, G, codes_c, n, n_q, q0, q1, K);
+    else
+      k_cross_terms<kCodeDim><<<blocks, CT_THREADS, 0, st>>>(p0, G, codes_c, n, n_q, q0, q1, K);
+    return cudaGetLastError();
+  };
+  if (d == kCodeDimSmall) {
+    const int bs = search8_block_stages(search8_split(n, sms));
+    const int nb = (n_q + bs - 1) / bs;
+    for (int b = 0; b < nb; ++b) {
+      const int q0 = (int)((int64_t)n_q * b / nb), q1 = (int)((int64_t)n_q * (b + 1) / nb);
+      if (q0 > 0 && (e = cross_terms(q0, q1)) != cudaSuccess) return e;
+      if ((e = launch_search8(dm, tables, p0, n, n_q, q0, q1, codes_c, status, sms, st)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  const int tiles = (int)((n + 127) / 128);
+  const int nkc = K / SR_KC;
   // one wave of CTA pairs: each tile's chunks split over two SMs; else, with
   // no more tiles than SMs, every item is split and the ring takes tile 1's areas
   const bool pairs = nkc % 4 == 0 && tiles <= max_search_clusters<2>();
@@ -1218,12 +1244,7 @@ cudaError_t launch_encode_chunk(const rvq_dims &dm, const void *tables, const fl
   const int nb = stage_blocks(n_q, own);
   for (int b = 0; b < nb; ++b) {
     const int q0 = (int)((int64_t)n_q * b / nb), q1 = (int)((int64_t)n_q * (b + 1) / nb);
-    if (q0 > 0) {
-      const int64_t threads = n * (q1 - q0) * 16;
-      k_cross_terms<<<(unsigned)((threads + CT_THREADS - 1) / CT_THREADS), CT_THREADS, 0, st>>>(p0, G, codes_c, n,
-                                                                                               n_q, q0, q1, K);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if (q0 > 0 && (e = cross_terms(q0, q1)) != cudaSuccess) return e;
     if (pairs) {
       e = launch_search_clusters<2>(p0, G, cb_img, cn, codes_c, n, n_q, q0, q1, K, tiles, dm.metric, status, st);
     } else {

@@ -119,8 +119,16 @@ cudaError_t stream_plan(const rvq_dims &dm, int n_q, int64_t n_frames, int64_t p
 // first kernel clears the status word (the caller has not).
 cudaError_t launch_encode_stream(const rvq_dims &dm, const void *tables, const float *x, int64_t n, int n_q,
                                  int32_t *codes, float *p0, int *status, bool zero_status, cudaStream_t s);
-cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q,
-                           int32_t *codes, int *status, int sms, cudaStream_t s);
+// The d = 8 stage loop over stages [q_begin, q_end) of n_q (a stage block;
+// the terms of earlier stages already subtracted from p0).
+cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q, int q_begin,
+                           int q_end, int32_t *codes, int *status, int sms, cudaStream_t s);
+// Whether the d = 8 search puts one tile on each CTA, split over its three
+// pipelines (no more tiles than SMs).
+inline bool search8_split(int64_t n, int sms) { return (n + 127) / 128 <= sms; }
+// The most stages a block of the d = 8 search spans: one stage's query terms
+// fit its pipeline's staging slots.
+int search8_block_stages(bool split);
 cudaError_t launch_decode(const rvq_dims &dm, const void *tables, const int32_t *codes, int64_t n,
                           int n_q, float *y, int64_t *bad, cudaStream_t s);
 

@@ -23,10 +23,14 @@
 //     end of each stage.  Pipeline 0 alone then builds the query (all three
 //     issuers read its TMEM columns) and gathers its terms.
 // Query terms are copied per thread -- its own frame's 32-byte rows -- by
-// 16-byte asynchronous copies into staging slots between distance chunks and
-// folded into an 8-float partial in registers one chunk later, in the order
-// P0, G[.][0], G[.][1], ...; the stage boundary loads the row of the code
-// just found straight into registers.  The distance of codeword k is
+// 16-byte asynchronous copies into staging slots after the first distance
+// chunk of a stage (all of them at once: one round trip a stage) and folded
+// into an 8-float partial in registers at the stage boundary, in the order
+// P0, G[.][0], G[.][1], ...; the boundary loads the row of the code just
+// found straight into registers.  Deep stacks run in blocks of at most as
+// many stages as a pipeline has staging slots (12 for a split tile, 4 for a
+// tile of its own), the terms of earlier blocks subtracted from P0 by
+// k_cross_terms between the launches.  The distance of codeword k is
 // -2 (s p).c_k + ||c_k||^2 with s = 1 (plain metric) or 1 / max(||p||, 1e-12)
 // (cosine metric, codebook normalised in the tables): the scale is applied to
 // the query before it is split, and the norms are added by a fourth MMA per
@@ -92,8 +96,8 @@ __device__ __forceinline__ float min64(const float (&v)[64]) {
 template <bool SPLIT>
 __global__ void __launch_bounds__(S8_THREADS, 1)
     k_search8_tc(const float *__restrict__ P0, const float *__restrict__ G, const float *__restrict__ cb_img,
-                 const float *__restrict__ cn_img, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int K,
-                 int n_tiles, int metric, int *__restrict__ status) {
+                 const float *__restrict__ cn_img, int32_t *__restrict__ codes, int64_t n_rows, int n_q, int q_begin,
+                 int q_end, int K, int n_tiles, int metric, int *__restrict__ status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
       uint32_t g = 0;  // stages gone through
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x)
-        for (int q = 0; q < n_q && ok; ++q, ++g) {
+        for (int q = q_begin; q < q_end && ok; ++q, ++g) {
           const int b = g & 1;
           if (g >= 2 && !mbar_wait(&bar.img_free[b], ((g >> 1) - 1) & 1)) {
             record_error8(status, RVQ_DEVICE_TIMEOUT);
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
       const uint32_t ta = tmem + (SPLIT ? 0 : p) * S8_PIPE_COLS;  // the query's columns
       const uint32_t buf0 = smem_addr(bufs);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x)
-        for (int q = 0; q < n_q && ok; ++q, ++g) {
+        for (int q = q_begin; q < q_end && ok; ++q, ++g) {
           const int b = g & 1;
           bool first = true;
           for (int c = SPLIT ? p : 0; c < nkc; c += SPLIT ? S8_P : 1) {
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
       return (item < n_items && nn < n_rows) ? nn : 0;
     };
     if (builder) {  // the first query's first term: the projection row itself
-      term_copy(0, P0 + row_of(blockIdx.x) * ld);
+      term_copy(0, P0 + row_of(blockIdx.x) * ld + q_begin * d);
       cp_async_commit();
       npend = 1;
       pend_p0 = true;
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
       const int64_t n_next = row_of(it + gridDim.x);
 #pragma unroll
       for (int j = 0; j < d; ++j) gl[j] = 0.0f;
-      for (int q = 0; q < n_q && ok; ++q, ++g) {
+      for (int q = q_begin; q < q_end && ok; ++q, ++g) {
         const int b = g & 1;
         if (builder) {
           // ---- stage boundary: query = partial - the row of the code just found
@@ -318,10 +322,10 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
           }
         }
         // ---- terms of the next query known before this stage's code:
-        //      next stage: P0[n][q+1], G[q+1][0..q-1];  next item: P0[n'][0]
-        const int q_next = q + 1 < n_q ? q + 1 : 0;
-        const int n_terms = !builder ? 0 : q + 1 < n_q ? q + 1 : (has_next ? 1 : 0);
-        const int64_t term_n = q + 1 < n_q ? n_row : n_next;
+        //      next stage: P0[n][q+1], G[q+1][q_begin..q-1];  next item: P0[n'][q_begin]
+        const int q_next = q + 1 < q_end ? q + 1 : q_begin;
+        const int n_terms = !builder ? 0 : q + 1 < q_end ? q + 1 - q_begin : (has_next ? 1 : 0);
+        const int64_t term_n = q + 1 < q_end ? n_row : n_next;
         int done = 0;
         // ---- scan this pipeline's chunks
         float best_v = __int_as_float(0x7f800000);
@@ -354,15 +358,18 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
               }
             }
           }
-          // ---- this chunk's share of the next query's known terms
+          // ---- this chunk's share of the next query's known terms: all of
+          //      them after the first chunk when the staging slots hold them
+          //      (one round trip a stage), else spread over the chunks
           if (n_terms > 0) {
-            const int target = (n_terms * (i_own + 1) + n_own - 1) / n_own;
+            const int target = n_terms <= kSlots ? n_terms : (n_terms * (i_own + 1) + n_own - 1) / n_own;
             while (done < target) {
               terms_finish();
               const int t1 = min(target, done + kSlots);
               for (int t = done; t < t1; ++t)
                 term_copy(t - done, t == 0 ? P0 + term_n * ld + q_next * d
-                                           : G + ((size_t)pair_index(q_next, t - 1) * K + my_codes[t - 1]) * d);
+                                           : G + ((size_t)pair_index(q_next, q_begin + t - 1) * K +
+                                                  my_codes[q_begin + t - 1]) * d);
               cp_async_commit();
               npend = t1 - done;
               pend_p0 = done == 0;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         }
         my_codes[q] = best_k;
         if (valid) codes[n * n_q + q] = best_k;
-        if (q + 1 < n_q) {  // the next query's last term
+        if (q + 1 < q_end) {  // the next query's last term
           const float4 *gr = reinterpret_cast<const float4 *>(G + ((size_t)pair_index(q + 1, q) * K + best_k) * d);
           const float4 a = __ldg(gr), c4 = __ldg(gr + 1);
           gl[0] = a.x;
@@ -451,20 +458,23 @@ static_assert(s8_smem_bytes(kMaxKSmall) <= 227 * 1024, "d = 8 search kernel shar
 
 }  // namespace
 
-cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q,
-                           int32_t *codes, int *status, int sms, cudaStream_t st) {
+int search8_block_stages(bool split) { return split ? S8_P * S8_TB : S8_TB; }
+
+cudaError_t launch_search8(const rvq_dims &dm, const void *tables, const float *p0, int64_t n, int n_q, int q_begin,
+                           int q_end, int32_t *codes, int *status, int sms, cudaStream_t st) {
   const TablesLayout L = tables_layout(dm);
   cudaError_t e = ensure_attributes8();
   if (e != cudaSuccess) return e;
   const int tiles = (int)((n + 127) / 128);
   // no more tiles than SMs: one tile per CTA, split between its three pipelines
-  const bool split = tiles <= sms;
+  const bool split = search8_split(n, sms);
   const int items = split ? tiles : (tiles + S8_P - 1) / S8_P;
   const int grid = items < sms ? items : sms;
   const size_t smem = s8_smem_bytes(dm.K);
   auto kern = split ? k_search8_tc<true> : k_search8_tc<false>;
   kern<<<grid, S8_THREADS, smem, st>>>(p0, at<float>(tables, L.g), at<float>(tables, L.cb_img),
-                                       at<float>(tables, L.cn_img8), codes, n, n_q, dm.K, tiles, dm.metric, status);
+                                       at<float>(tables, L.cn_img8), codes, n, n_q, q_begin, q_end, dm.K, tiles,
+                                       dm.metric, status);
   return cudaGetLastError();
 }
 

@@ -226,18 +226,21 @@ def test_tiles_on_clusters(K, Q, N, metric):
         rq.rvq_set_stream_max_frames(prev)
 
 
-@pytest.mark.parametrize("K,Q,N,metric", [(512, 20, 3000, "l2"), (768, 20, 3000, "l2"), (768, 13, 2000, "cosine"),
-                                          (1024, 17, 155 * 128 - 40, "l2")])
-def test_deep_stacks_in_stage_blocks(K, Q, N, metric):
-    """Stacks deeper than eight stages whose terms outnumber a pipeline's
+@pytest.mark.parametrize("K,Q,N,metric,d", [(512, 20, 3000, "l2", 64), (768, 20, 3000, "l2", 64),
+                                            (768, 13, 2000, "cosine", 64), (1024, 17, 155 * 128 - 40, "l2", 64),
+                                            (1024, 20, 3000, "cosine", 8), (512, 13, 160 * 128 - 7, "l2", 8)])
+def test_deep_stacks_in_stage_blocks(K, Q, N, metric, d):
+    """Stacks deeper than six stages whose terms outnumber a pipeline's
     chunks run as several search launches over blocks of stages, the terms of
     earlier blocks subtracted from the projections in between: on CTA pairs
-    (K = 512), split items (K = 768) and two-tile items (155 tiles, more than
-    the SMs), with ragged blocks (20 = 6 + 7 + 7, 13 = 6 + 7, 17 = 5 + 6 + 6).
+    (K = 512), split items (K = 768; d = 8 at 3000 frames) and items of two
+    (d = 64) or three (d = 8) tiles when the tiles outnumber the SMs, in
+    blocks (d = 64: 20 = 5 + 5 + 5 + 5, 13 = 4 + 4 + 5, 17 = 5 + 6 + 6; d = 8:
+    20 = 10 + 10 on split tiles, 13 = 3 + 3 + 3 + 4 on tiles of their own).
     The tile kernels are forced; every frame is checked."""
     prev = rq.rvq_set_stream_max_frames(0)
     try:
-        w, W = _small_weights(D=64, K=K, Q=Q, seed=K + Q, bias=True, decay=0.9)
+        w, W = _small_weights(D=64, K=K, Q=Q, seed=K + Q, bias=True, decay=0.9, d=d)
         x = np.random.default_rng(K + N).standard_normal((N, 64)).astype(np.float32)
         run_small(W, x, label=f"K={K} Q={Q} N={N} {metric}", metric=metric)
     finally:
