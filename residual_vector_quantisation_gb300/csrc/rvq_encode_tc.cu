@@ -39,7 +39,9 @@ using namespace ptx;
 // CTA item: NT tiles of 128 frames x NC output columns (NT = 2, NC = 256 for
 // large calls; one tile and 128 or 64 columns when a call has too few such
 // items to fill the GPU), K = D in slices of 16 floats (64-byte rows, 64-byte
-// swizzle), 3-stage TMA ring.
+// swizzle), 3-stage TMA ring.  The smaller items keep two accumulators in
+// TMEM, so an item's epilogue overlaps the next item's MMAs (moss_lfq encode
+// 268 -> 259 us).
 // Warps: 0 and 6 TMA producers (x tiles; w_in hi and lo tiles -- a thread's
 // copies are carried out one after another, so two threads issue them),
 // 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
@@ -55,14 +57,18 @@ struct PjShape {
   static constexpr uint32_t STAGE = 2 * NT * PJ_A_TILE + 2 * B;      // raw[NT] lo[NT] bhi blo
   static constexpr uint32_t TX_X = NT * PJ_A_TILE;                   // bytes each producer's TMA writes per stage
   static constexpr uint32_t TX_W = 2 * B;
-  static constexpr uint32_t TMEM_COLS = NT * NC;
+  static constexpr uint32_t ACC_COLS = NT * NC;                      // one item's accumulators
+  // two accumulators when they fit TMEM, so an item's epilogue overlaps the
+  // next item's MMAs
+  static constexpr uint32_t ACC_BUFS = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = ACC_BUFS * ACC_COLS;
   static constexpr uint32_t IDESC = idesc_tf32(128, NC);
   static constexpr int ROWS = 128 * NT;                              // frames per item
 };
 
 struct PjBars {
   uint64_t full[PJ_STAGES], conv[PJ_STAGES], empty[PJ_STAGES];
-  uint64_t acc_full, acc_empty, drain;
+  uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem;
 };
 template <int NT, int NC>
@@ -99,8 +105,10 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       mbar_init(&bar.conv[s], 128);
       mbar_init(&bar.empty[s], 1);
     }
-    mbar_init(&bar.acc_full, 1);
-    mbar_init(&bar.acc_empty, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar.acc_full[b], 1);
+      mbar_init(&bar.acc_empty[b], 128);
+    }
     mbar_init(&bar.drain, 1);
     fence_mbar_init();
     prefetch_tmap(&tm_x);
@@ -155,7 +163,8 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       uint32_t it = 0, n_done = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n_done) {
-        if (n_done > 0 && !mbar_wait(&bar.acc_empty, (n_done - 1) & 1)) {
+        const uint32_t ab = n_done % S::ACC_BUFS, au = n_done / S::ACC_BUFS;  // accumulator, its use
+        if (au > 0 && !mbar_wait(&bar.acc_empty[ab], (au - 1) & 1)) {
           record_error(status, RVQ_DEVICE_TIMEOUT);
           ok = false;
           break;
@@ -177,14 +186,14 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
               const uint64_t al = smem_desc(smem_addr(a_lo(s, t)) + j * 32, 16, 512, kSwizzle64B);
               const uint64_t bh = smem_desc(smem_addr(b_hi(s)) + j * 32, 16, 512, kSwizzle64B);
               const uint64_t bl = smem_desc(smem_addr(b_lo(s)) + j * 32, 16, 512, kSwizzle64B);
-              const uint32_t d = tmem + t * NC;
+              const uint32_t d = tmem + ab * S::ACC_COLS + t * NC;
               mma_tf32(d, ah, bh, S::IDESC, (ks | j) ? 1u : 0u);
               mma_tf32(d, ah, bl, S::IDESC, 1u);
               mma_tf32(d, al, bh, S::IDESC, 1u);
             }
           mma_commit(&bar.empty[s]);
         }
-        if (ok) mma_commit(&bar.acc_full);
+        if (ok) mma_commit(&bar.acc_full[ab]);
       }
       // no MMA of this CTA may be in flight when TMEM is freed
       mma_commit(&bar.drain);
@@ -195,11 +204,57 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     const int ct = tid - 64;                 // 0..127
     const int quarter = warp & 3;            // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;       // row within each tile
+    // One epilogue step: 32 columns of one tile of an item's accumulator,
+    // + bias, to P0 (e < NT * NC / 32).
+    constexpr int NE = NT * NC / 32;
+    auto epi_step = [&](int item_e, uint32_t ab, int e) {
+      const int64_t n = (int64_t)(item_e / n_cb) * S::ROWS + (e / (NC / 32)) * 128 + r;
+      const int c0 = (item_e % n_cb) * NC, c = (e % (NC / 32)) * 32;
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + ab * S::ACC_COLS + (e / (NC / 32)) * NC + c, v);
+      tmem_wait_ld();
+      if (n < n_rows && c0 + c < n_cols) {
+        // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
+        float *out = P0 + n * n_cols + c0 + c;
+        const int n4 = min(8, (n_cols - (c0 + c)) / 4);
+        const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0 + c);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (u < n4) {
+            const float4 b = __ldg(b4 + u);
+            reinterpret_cast<float4 *>(out)[u] =
+                make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
+          }
+        }
+      }
+    };
+    // With two accumulators, an item's epilogue is done a step at a time
+    // between the lo splits of the next item (once its MMAs are seen
+    // complete), so the tensor core does not wait for it; with one, the
+    // next item's MMAs need the accumulator, and it is done at once.
+    int pend = -1, pend_done = 0;        // the item whose epilogue is pending, steps done
+    uint32_t pend_ab = 0, pend_au = 0;   // its accumulator and that accumulator's use
+    bool pend_ready = false;             // its MMAs are seen complete
+    auto finish_pending = [&]() -> bool {
+      if (pend < 0) return true;
+      // warp-uniform decision before the warp-collective TMEM loads
+      if (!pend_ready) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full[pend_ab], pend_au & 1))) {
+          record_error(status, RVQ_DEVICE_TIMEOUT);
+          return false;
+        }
+        tc_fence_after();
+      }
+#pragma unroll 1
+      for (; pend_done < NE; ++pend_done) epi_step(pend, pend_ab, pend_done);
+      tc_fence_before();
+      mbar_arrive(&bar.acc_empty[pend_ab]);
+      pend = -1;
+      return true;
+    };
     uint32_t it = 0, n_done = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++n_done) {
-      const int64_t m0 = (int64_t)(item / n_cb) * S::ROWS;
-      const int c0 = (item % n_cb) * NC;
       for (int ks = 0; ks < nk; ++ks, ++it) {
         const int s = it % PJ_STAGES;
         if (!__all_sync(0xffffffffu, mbar_wait(&bar.full[s], (it / PJ_STAGES) & 1))) {
@@ -222,41 +277,30 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bar.conv[s]);
-      }
-      if (!ok) break;
-      // warp-uniform decision before the warp-collective TMEM loads
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full, n_done & 1))) {
-        record_error(status, RVQ_DEVICE_TIMEOUT);
-        break;
-      }
-      tc_fence_after();
-#pragma unroll 1
-      for (int t = 0; t < NT; ++t) {
-        const int64_t n = m0 + t * 128 + r;
-        float *out = P0 + n * n_cols + c0;
-#pragma unroll 1
-        for (int c = 0; c < NC; c += 32) {
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + t * NC + c, v);
-          tmem_wait_ld();
-          if (n < n_rows && c0 + c < n_cols) {
-            // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
-            const int n4 = min(8, (n_cols - (c0 + c)) / 4);
-            const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0 + c);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              if (u < n4) {
-                const float4 b = __ldg(b4 + u);
-                reinterpret_cast<float4 *>(out + c)[u] =
-                    make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
-              }
-            }
+        if (S::ACC_BUFS == 2 && pend >= 0 && pend_done < NE) {
+          if (!pend_ready) {
+            pend_ready = __all_sync(0xffffffffu, mbar_test_wait(&bar.acc_full[pend_ab], pend_au & 1));
+            if (pend_ready) tc_fence_after();
           }
+          if (pend_ready) epi_step(pend, pend_ab, pend_done++);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bar.acc_empty);
+      if (!ok) break;
+      if (!finish_pending()) {  // the previous item's epilogue (two accumulators)
+        ok = false;
+        break;
+      }
+      pend = item;
+      pend_ab = n_done % S::ACC_BUFS;
+      pend_au = n_done / S::ACC_BUFS;
+      pend_done = 0;
+      pend_ready = false;
+      if (S::ACC_BUFS == 1 && !finish_pending()) {  // one accumulator: this item's epilogue now
+        ok = false;
+        break;
+      }
     }
+    if (ok) finish_pending();  // the last item's
   }
   tc_fence_before();
   __syncthreads();
@@ -1147,7 +1191,10 @@ int sm_count() {
 // cycles of an item's K-slice: 12 MMAs of 128 x 256 x 8 at 128 cycles, 6 of
 // 128 x 128 x 8 at 64, 6 of 128 x 64 x 8 at 48), small items in at most two
 // waves: more re-read x and w_in from L2 more often than they save (three
-// waves measured 470 against 443 us for 9728 frames of ten 4096-entry stages).
+// waves measured 470 against 443 us for 9728 frames of ten 4096-entry
+// stages).  (Items of 256 x 128, two accumulators in TMEM, measured slower
+// wherever this count favoured them: moss_deep encode 704 against 686 us;
+// forced onto large_batch, 1.70 against 1.46 ms.)
 int projection_shape(int64_t n, int n_cols, int sms) {
   const int64_t t128 = (n + 127) / 128;
   const int64_t items[3] = {((n + 255) / 256) * ((n_cols + 255) / 256), t128 * ((n_cols + 127) / 128),
