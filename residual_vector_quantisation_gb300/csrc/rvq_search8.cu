@@ -61,6 +61,7 @@ constexpr uint32_t S8_HALF = 128 * S8_D * 4;     // 4 KB: the hi or the lo block
 constexpr int S8_TB = 4;                         // staging slots per pipeline
 constexpr uint32_t S8_STG_BYTES = S8_P * S8_TB * 2 * 128 * 16;  // [pipe][slot][half][frame] x 16 B
 constexpr uint32_t S8_XCH_BYTES = 2 * 2 * 128 * 4 * 2;  // values, indices
+constexpr uint32_t S8_XROW_BYTES = 2 * 128 * S8_D * 4;  // pipelines 1, 2: their candidates' next-term rows
 
 struct S8Bars {
   uint64_t img_full[2], img_free[2];
@@ -75,7 +76,7 @@ __host__ __device__ constexpr uint32_t s8_buf_stride(int K) {
   return ((uint32_t)K * (2 * S8_D * 4) + (uint32_t)cn_img8_blocks(K) * S8_NBLOCK + 1023u) & ~1023u;
 }
 __host__ __device__ constexpr size_t s8_smem_bytes(int K) {
-  return 1024 + 2 * (size_t)s8_buf_stride(K) + S8_STG_BYTES + S8_XCH_BYTES + sizeof(S8Bars);
+  return 1024 + 2 * (size_t)s8_buf_stride(K) + S8_STG_BYTES + S8_XCH_BYTES + S8_XROW_BYTES + sizeof(S8Bars);
 }
 
 __device__ __forceinline__ void record_error8(int *status, int code) { atomicCAS(status, 0, code); }
@@ -111,7 +112,8 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
   unsigned char *stg = smem + 2 * buf_stride;
   float *xv = reinterpret_cast<float *>(stg + S8_STG_BYTES);  // [2][2][128]
   int *xk = reinterpret_cast<int *>(xv + 2 * 2 * 128);         // [2][2][128]
-  S8Bars &bar = *reinterpret_cast<S8Bars *>(xk + 2 * 2 * 128);
+  float4 *xr = reinterpret_cast<float4 *>(xk + 2 * 2 * 128);   // [2][128][2]: one buffer (see the exchange)
+  S8Bars &bar = *reinterpret_cast<S8Bars *>(xr + 2 * 128 * 2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = (n_tiles + T - 1) / T;
   // one tile per CTA in the SPLIT variant
@@ -379,8 +381,18 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
         }
         if (!ok) break;
         mbar_arrive(&bar.img_free[b]);  // (kept in the count: every row thread is done with the stage)
+        // the next query's last term for this pipeline's candidate code, loaded
+        // before the exchange so that its latency overlaps it (the winner's row
+        // is then at hand when the code is known)
+        const bool next_term = q + 1 < q_end;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c4 = a;
+        if (next_term) {
+          const float4 *gr = reinterpret_cast<const float4 *>(G + ((size_t)pair_index(q + 1, q) * K + best_k) * d);
+          a = __ldg(gr);
+          c4 = __ldg(gr + 1);
+        }
         if (SPLIT) {
-          // ---- pipelines 1, 2 hand their minima to pipeline 0
+          // ---- pipelines 1, 2 hand their minima (and candidate rows) to pipeline 0
           const int xb = xu & 1;
           const uint32_t use = xu >> 1;
           ++xu;
@@ -392,6 +404,12 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             }
             xv[(xb * 2 + p - 1) * 128 + f] = best_v;
             xk[(xb * 2 + p - 1) * 128 + f] = best_k;
+            // one buffer: pipeline 0 reads it before it builds the next query,
+            // which this pipeline waits for before its next write
+            if (next_term) {
+              xr[((p - 1) * 128 + f) * 2] = a;
+              xr[((p - 1) * 128 + f) * 2 + 1] = c4;
+            }
             mbar_arrive(&bar.xch_full[xb]);
             continue;
           }
@@ -400,6 +418,7 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             ok = false;
             break;
           }
+          int from = 0;  // the pipeline whose candidate won
 #pragma unroll
           for (int pp = 0; pp < 2; ++pp) {
             const float ov = xv[(xb * 2 + pp) * 128 + f];
@@ -407,15 +426,18 @@ __global__ void __launch_bounds__(S8_THREADS, 1)
             if (ov < best_v || (ov == best_v && ok_k < best_k)) {
               best_v = ov;
               best_k = ok_k;
+              from = pp + 1;
             }
+          }
+          if (next_term && from > 0) {
+            a = xr[((from - 1) * 128 + f) * 2];
+            c4 = xr[((from - 1) * 128 + f) * 2 + 1];
           }
           mbar_arrive(&bar.xch_free[xb]);
         }
         my_codes[q] = best_k;
         if (valid) codes[n * n_q + q] = best_k;
-        if (q + 1 < q_end) {  // the next query's last term
-          const float4 *gr = reinterpret_cast<const float4 *>(G + ((size_t)pair_index(q + 1, q) * K + best_k) * d);
-          const float4 a = __ldg(gr), c4 = __ldg(gr + 1);
+        if (next_term) {  // the next query's last term
           gl[0] = a.x;
           gl[1] = a.y;
           gl[2] = a.z;
