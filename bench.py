@@ -45,8 +45,8 @@ METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
 # hold the commands and the figures.
 TRAFFIC = {
     ("encode", "large_batch"): {
-        "bytes_per_frame": (826.98e6 + 358.17e6 + 429.68e6 + 8.05e6) / 192000,
-        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu": "06cdf7acce6c9fbf",
+        "bytes_per_frame": (827.52e6 + 357.96e6 + 428.56e6 + 9.32e6) / 192000,
+        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu": "c3c7bac6623d2198",
                     "residual_vector_quantisation_gb300/csrc/rvq_api.cu": "4f5bf68560f9671d"},
         "profile": "profiles/encode_tc_large_batch.md"},
     ("decode", "large_batch"): {
