@@ -336,8 +336,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 // the row warps gather those rows between distance chunks: 16-byte
 // asynchronous copies (four lanes per 64-byte row segment) into the staging
 // area, subtracted from the partial sum one chunk later (the P0 row is copied
-// straight into the partial); the stage boundary loads only the one row of
-// the code just found, straight into registers, and forms the query there.
+// straight into the partial); at the stage boundary the staging area takes
+// the one row of the code just found, copied the same way, and the query is
+// formed in registers.
 // Terms are added in the order s = 0, 1, ..., q.  A launch over a block of
 // stages [q_begin, q_end) of a deep stack finds the terms of the earlier
 // blocks already subtracted from P0 (k_cross_terms) and sums from q_begin.
