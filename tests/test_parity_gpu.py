@@ -247,6 +247,29 @@ def test_deep_stacks_in_stage_blocks(K, Q, N, metric, d):
         rq.rvq_set_stream_max_frames(prev)
 
 
+@pytest.mark.parametrize("K,Q,d,prefixes", [(768, 13, 64, (8, 6)), (1024, 20, 8, (12, 10))])
+def test_stage_blocks_keep_the_unblocked_sums(K, Q, d, prefixes):
+    """The terms of earlier stage blocks are subtracted from P0 in the order
+    the search continues in, so a blocked call reproduces the sums of an
+    unblocked one bit for bit: the codes of every prefix depth equal the first
+    stages of the full depth exactly, whether the prefix call is blocked the
+    same way (d = 64: 13 = 4 + 4 + 5 and 8 = 4 + 4; d = 8: 20 = 10 + 10 and
+    12 in one block) or not at all (d = 64, 6 stages; d = 8, the first 10)."""
+    prev = rq.rvq_set_stream_max_frames(0)
+    try:
+        w, W = _small_weights(D=64, K=K, Q=Q, seed=K + Q + d, bias=True, decay=0.9, d=d)
+        x = np.random.default_rng(Q).standard_normal((2000, 64)).astype(np.float32)
+        rvq = make_rvq(W)
+        xt = torch.from_numpy(x).to(DEV)
+        full = rvq.encode(xt).cpu().numpy()
+        for n_q in prefixes:
+            part = rvq.encode(xt, n_q).cpu().numpy()
+            assert np.array_equal(part, full[:, :n_q]), f"prefix {n_q} of {Q}"
+        check_encode(W, x, full, label=f"K={K} Q={Q} d={d}")
+    finally:
+        rq.rvq_set_stream_max_frames(prev)
+
+
 def test_biases_and_prefix_depths():
     w, W = _small_weights(D=256, K=512, Q=6, bias=True)
     x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
