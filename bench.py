@@ -50,8 +50,8 @@ TRAFFIC = {
                     "residual_vector_quantisation_gb300/csrc/rvq_api.cu": "4f5bf68560f9671d"},
         "profile": "profiles/encode_tc_large_batch.md"},
     ("decode", "large_batch"): {
-        "bytes_per_frame": (52.87e6 + 738.77e6) / 192000,
-        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_decode.cu": "52de1449207f122f"},
+        "bytes_per_frame": (52.49e6 + 738.71e6) / 192000,
+        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_decode.cu": "c5dbdfd597ff2668"},
         "profile": "profiles/decode_large_batch.md"},
 }
 L2_BYTES = 129 * 2 ** 20
