@@ -50,6 +50,7 @@ constexpr int PJ_BK = 16;
 constexpr int PJ_STAGES = 3;
 constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;  // 8 KB: one tile's K-slice
 constexpr int PJ_THREADS = 224;
+constexpr uint32_t PJ_EPI = 4 * 32 * 32 * 4;    // a 32 x 32 block per epilogue warp
 
 template <int NT, int NC>
 struct PjShape {
@@ -72,7 +73,7 @@ struct PjBars {
   uint32_t tmem;
 };
 template <int NT, int NC>
-constexpr size_t pj_smem() { return 1024 + PJ_STAGES * PjShape<NT, NC>::STAGE + sizeof(PjBars); }
+constexpr size_t pj_smem() { return 1024 + PJ_STAGES * PjShape<NT, NC>::STAGE + PJ_EPI + sizeof(PjBars); }
 
 __device__ __forceinline__ void record_error(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
-  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * S::STAGE);
+  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * S::STAGE + PJ_EPI);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_launch_dependents();
   if (zero_status && blockIdx.x == 0 && tid == 0) *status = 0;
@@ -203,30 +204,42 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     // ---------------- lo split + epilogue (warps 2..5) ----------------
     const int ct = tid - 64;                 // 0..127
     const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;       // row within each tile
+    // this warp's 32 x 32 block: row i's 16-byte piece j at i * 8 + (j ^ (i & 7)),
+    // so both the row-wise writes and the column-wise reads below are free of
+    // bank conflicts
+    float4 *blk = reinterpret_cast<float4 *>(smem + PJ_STAGES * S::STAGE) + (warp - 2) * 256;
     // One epilogue step: 32 columns of one tile of an item's accumulator,
-    // + bias, to P0 (e < NT * NC / 32).
+    // + bias, to P0 (e < NT * NC / 32).  Lane i holds row i of the warp's 32
+    // rows; the block goes through shared memory so that each store
+    // instruction writes four whole 128-byte row pieces (lane i: row
+    // 4u + i / 8, piece i % 8) instead of 32 pieces of 16 bytes in 32 lines
+    // (large_batch encode about 5 % faster).
     constexpr int NE = NT * NC / 32;
     auto epi_step = [&](int item_e, uint32_t ab, int e) {
-      const int64_t n = (int64_t)(item_e / n_cb) * S::ROWS + (e / (NC / 32)) * 128 + r;
+      const int64_t n0 = (int64_t)(item_e / n_cb) * S::ROWS + (e / (NC / 32)) * 128 + quarter * 32;
       const int c0 = (item_e % n_cb) * NC, c = (e % (NC / 32)) * 32;
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + ab * S::ACC_COLS + (e / (NC / 32)) * NC + c, v);
       tmem_wait_ld();
-      if (n < n_rows && c0 + c < n_cols) {
-        // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
-        float *out = P0 + n * n_cols + c0 + c;
-        const int n4 = min(8, (n_cols - (c0 + c)) / 4);
-        const float4 *b4 = reinterpret_cast<const float4 *>(bias + c0 + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        blk[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      __syncwarp();
+      // n_cols is a multiple of 8 (n_q * d): a group may end inside the row
+      const int pc = lane & 7;
+      if (c0 + c < n_cols && pc < min(8, (n_cols - (c0 + c)) / 4)) {
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(bias + c0 + c) + pc);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          if (u < n4) {
-            const float4 b = __ldg(b4 + u);
-            reinterpret_cast<float4 *>(out)[u] =
-                make_float4(v[4 * u] + b.x, v[4 * u + 1] + b.y, v[4 * u + 2] + b.z, v[4 * u + 3] + b.w);
+          const int i = 4 * u + (lane >> 3);
+          if (n0 + i < n_rows) {
+            const float4 a = blk[i * 8 + (pc ^ (i & 7))];
+            reinterpret_cast<float4 *>(P0 + (n0 + i) * n_cols + c0 + c)[pc] =
+                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
           }
         }
       }
+      __syncwarp();  // the block is read before the next step writes it
     };
     // With two accumulators, an item's epilogue is done a step at a time
     // between the lo splits of the next item (once its MMAs are seen
