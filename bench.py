@@ -45,8 +45,8 @@ METRIC = "RVQ encode & decode frames/s (Q=8,K=1024,d=64,D=1024); % of roofline"
 # hold the commands and the figures.
 TRAFFIC = {
     ("encode", "large_batch"): {
-        "bytes_per_frame": (827.29e6 + 359.63e6 + 428.56e6 + 9.29e6) / 192000,
-        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu": "31503a0cf5ff89d9",
+        "bytes_per_frame": (827.76e6 + 359.98e6 + 428.53e6 + 9.26e6) / 192000,
+        "sources": {"residual_vector_quantisation_gb300/csrc/rvq_encode_tc.cu": "ae1e8ed6756079cb",
                     "residual_vector_quantisation_gb300/csrc/rvq_api.cu": "4f5bf68560f9671d"},
         "profile": "profiles/encode_tc_large_batch.md"},
     ("decode", "large_batch"): {

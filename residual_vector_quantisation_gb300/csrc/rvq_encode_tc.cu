@@ -44,13 +44,15 @@ using namespace ptx;
 // 268 -> 259 us).
 // Warps: 0 and 6 TMA producers (x tiles; w_in hi and lo tiles -- a thread's
 // copies are carried out one after another, so two threads issue them),
-// 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue.
+// 1 MMA issuer (+ TMEM owner), 2-5 lo-split + epilogue, and for the 256 x 256
+// items, whose one accumulator makes the next item's MMAs wait for the
+// epilogue, 7-10 a second epilogue crew that takes the second tile's steps
+// (large_batch encode 1.406 -> 1.381 ms).
 // ===========================================================================
 constexpr int PJ_BK = 16;
 constexpr int PJ_STAGES = 3;
 constexpr uint32_t PJ_A_TILE = 128 * PJ_BK * 4;  // 8 KB: one tile's K-slice
-constexpr int PJ_THREADS = 224;
-constexpr uint32_t PJ_EPI = 4 * 32 * 32 * 4;    // a 32 x 32 block per epilogue warp
+constexpr uint32_t PJ_BLK = 32 * 32 * 4;       // a 32 x 32 block per epilogue warp
 
 template <int NT, int NC>
 struct PjShape {
@@ -65,6 +67,10 @@ struct PjShape {
   static constexpr uint32_t TMEM_COLS = ACC_BUFS * ACC_COLS;
   static constexpr uint32_t IDESC = idesc_tf32(128, NC);
   static constexpr int ROWS = 128 * NT;                              // frames per item
+  // one-accumulator items: four more warps share the epilogue
+  static constexpr int HELP = ACC_BUFS == 1 ? 4 : 0;
+  static constexpr int THREADS = 224 + 32 * HELP;
+  static constexpr uint32_t EPI = (4 + HELP) * PJ_BLK;
 };
 
 struct PjBars {
@@ -73,7 +79,7 @@ struct PjBars {
   uint32_t tmem;
 };
 template <int NT, int NC>
-constexpr size_t pj_smem() { return 1024 + PJ_STAGES * PjShape<NT, NC>::STAGE + PJ_EPI + sizeof(PjBars); }
+constexpr size_t pj_smem() { return 1024 + PJ_STAGES * PjShape<NT, NC>::STAGE + PjShape<NT, NC>::EPI + sizeof(PjBars); }
 
 __device__ __forceinline__ void record_error(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -81,7 +87,7 @@ __device__ __forceinline__ void record_error(int *status, int code) { atomicCAS(
 // is); the kernel also lets a dependent launch start at once (programmatic
 // dependent launch; no effect on a plain launch after it).
 template <int NT, int NC>
-__global__ void __launch_bounds__(PJ_THREADS, 1)
+__global__ void __launch_bounds__(PjShape<NT, NC>::THREADS, 1)
     k_project_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_whi,
                  const __grid_constant__ CUtensorMap tm_wlo, const float *__restrict__ bias,
                  float *__restrict__ P0, int64_t n_rows, int n_cols, int D, int n_items, int n_cb,
@@ -90,7 +96,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
-  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * S::STAGE + PJ_EPI);
+  PjBars &bar = *reinterpret_cast<PjBars *>(smem + PJ_STAGES * S::STAGE + S::EPI);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_launch_dependents();
   if (zero_status && blockIdx.x == 0 && tid == 0) *status = 0;
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar.acc_full[b], 1);
-      mbar_init(&bar.acc_empty[b], 128);
+      mbar_init(&bar.acc_empty[b], S::HELP ? 256 : 128);
     }
     mbar_init(&bar.drain, 1);
     fence_mbar_init();
@@ -125,6 +131,64 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem;
 
+  // this warp's 32 x 32 block: row i's 16-byte piece j at i * 8 + (j ^ (i & 7)),
+  // so both the row-wise writes and the column-wise reads below are free of
+  // bank conflicts
+  const int quarter = warp & 3;  // TMEM lanes this warp may access (epilogue warps)
+  const int ew = warp >= 2 && warp <= 5 ? warp - 2 : warp >= 7 ? warp - 3 : 0;  // epilogue warp index
+  float4 *blk = reinterpret_cast<float4 *>(smem + PJ_STAGES * S::STAGE) + ew * 256;
+  // One epilogue step: 32 columns of one tile of an item's accumulator,
+  // + bias, to P0 (e < NT * NC / 32).  Lane i holds row i of the warp's 32
+  // rows; the block goes through shared memory so that each store
+  // instruction writes four whole 128-byte row pieces (lane i: row
+  // 4u + i / 8, piece i % 8) instead of 32 pieces of 16 bytes in 32 lines.
+  // A 256 x 256 item keeps one accumulator, so the next item's MMAs wait
+  // for its epilogue: large_batch encode 1.465 -> 1.416 ms with the block
+  // transpose, -> 1.394 ms with the bias loads out of the steps' dependency
+  // chain.  (A TMA store of each block, the bias added before the block is
+  // written, measured the same: 1.403-1.405 against 1.405-1.412 ms.)
+  constexpr int NE = NT * NC / 32, NCS = NC / 32;
+  const int pc = lane & 7;
+  // this lane's four bias values of step e (zero past the last column; n_cols
+  // is a multiple of 8, n_q * d, so a step may end inside the row)
+  auto bias4 = [&](int item_e, int e) {
+    const int cc = (item_e % n_cb) * NC + (e % NCS) * 32;
+    return cc < n_cols && pc < min(8, (n_cols - cc) / 4) ? __ldg(reinterpret_cast<const float4 *>(bias + cc) + pc)
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto epi_load = [&](uint32_t ab, int e, float (&v)[32]) {
+    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + ab * S::ACC_COLS + (e / NCS) * NC + (e % NCS) * 32, v);
+  };
+  // v (loaded and waited for) + b to P0
+  auto epi_put = [&](int item_e, int e, const float (&v)[32], float4 b) {
+    const int64_t n0 = (int64_t)(item_e / n_cb) * S::ROWS + (e / NCS) * 128 + quarter * 32;
+    const int c0 = (item_e % n_cb) * NC, c = (e % NCS) * 32;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      blk[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    if (c0 + c < n_cols && pc < min(8, (n_cols - (c0 + c)) / 4)) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = 4 * u + (lane >> 3);
+        if (n0 + i < n_rows) {
+          const float4 a = blk[i * 8 + (pc ^ (i & 7))];
+          reinterpret_cast<float4 *>(P0 + (n0 + i) * n_cols + c0 + c)[pc] =
+              make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        }
+      }
+    }
+    __syncwarp();  // the block is read before the next step writes it
+  };
+  // a single step (two-accumulator items, between lo splits), its bias load
+  // overlapping the TMEM load
+  auto epi_step = [&](int item_e, uint32_t ab, int e) {
+    float v[32];
+    epi_load(ab, e, v);
+    const float4 b = bias4(item_e, e);
+    tmem_wait_ld();
+    epi_put(item_e, e, v, b);
+  };
   if (warp == 0 || warp == 6) {
     // ---------------- TMA producers ----------------
     const bool px = warp == 0;
@@ -200,66 +264,9 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       mma_commit(&bar.drain);
       mbar_wait(&bar.drain, 0);
     }
-  } else {
+  } else if (warp <= 5) {
     // ---------------- lo split + epilogue (warps 2..5) ----------------
     const int ct = tid - 64;                 // 0..127
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    // this warp's 32 x 32 block: row i's 16-byte piece j at i * 8 + (j ^ (i & 7)),
-    // so both the row-wise writes and the column-wise reads below are free of
-    // bank conflicts
-    float4 *blk = reinterpret_cast<float4 *>(smem + PJ_STAGES * S::STAGE) + (warp - 2) * 256;
-    // One epilogue step: 32 columns of one tile of an item's accumulator,
-    // + bias, to P0 (e < NT * NC / 32).  Lane i holds row i of the warp's 32
-    // rows; the block goes through shared memory so that each store
-    // instruction writes four whole 128-byte row pieces (lane i: row
-    // 4u + i / 8, piece i % 8) instead of 32 pieces of 16 bytes in 32 lines.
-    // A 256 x 256 item keeps one accumulator, so the next item's MMAs wait
-    // for its epilogue: large_batch encode 1.465 -> 1.416 ms with the block
-    // transpose, -> 1.394 ms with the bias loads out of the steps' dependency
-    // chain.  (A TMA store of each block, the bias added before the block is
-    // written, measured the same: 1.403-1.405 against 1.405-1.412 ms.)
-    constexpr int NE = NT * NC / 32, NCS = NC / 32;
-    const int pc = lane & 7;
-    // this lane's four bias values of step e (zero past the last column; n_cols
-    // is a multiple of 8, n_q * d, so a step may end inside the row)
-    auto bias4 = [&](int item_e, int e) {
-      const int cc = (item_e % n_cb) * NC + (e % NCS) * 32;
-      return cc < n_cols && pc < min(8, (n_cols - cc) / 4) ? __ldg(reinterpret_cast<const float4 *>(bias + cc) + pc)
-                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    auto epi_load = [&](uint32_t ab, int e, float (&v)[32]) {
-      tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + ab * S::ACC_COLS + (e / NCS) * NC + (e % NCS) * 32, v);
-    };
-    // v (loaded and waited for) + b to P0
-    auto epi_put = [&](int item_e, int e, const float (&v)[32], float4 b) {
-      const int64_t n0 = (int64_t)(item_e / n_cb) * S::ROWS + (e / NCS) * 128 + quarter * 32;
-      const int c0 = (item_e % n_cb) * NC, c = (e % NCS) * 32;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        blk[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      __syncwarp();
-      if (c0 + c < n_cols && pc < min(8, (n_cols - (c0 + c)) / 4)) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = 4 * u + (lane >> 3);
-          if (n0 + i < n_rows) {
-            const float4 a = blk[i * 8 + (pc ^ (i & 7))];
-            reinterpret_cast<float4 *>(P0 + (n0 + i) * n_cols + c0 + c)[pc] =
-                make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-          }
-        }
-      }
-      __syncwarp();  // the block is read before the next step writes it
-    };
-    // a single step (two-accumulator items, between lo splits), its bias load
-    // overlapping the TMEM load
-    auto epi_step = [&](int item_e, uint32_t ab, int e) {
-      float v[32];
-      epi_load(ab, e, v);
-      const float4 b = bias4(item_e, e);
-      tmem_wait_ld();
-      epi_put(item_e, e, v, b);
-    };
     // With two accumulators, an item's epilogue is done a step at a time
     // between the lo splits of the next item (once its MMAs are seen
     // complete), so the tensor core does not wait for it; with one, the
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 #pragma unroll
       for (int k = 0; k < NCS; ++k) bq[k] = bias4(pend, k);
 #pragma unroll
-      for (int e = 0; e < NE; ++e) {
+      for (int e = 0; e < (S::HELP ? NE / 2 : NE); ++e) {
         if (e < pend_done) continue;
         float v[32];
         epi_load(pend_ab, e, v);
@@ -345,6 +352,29 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
       }
     }
     if (ok) finish_pending();  // the last item's
+  } else if (S::HELP) {
+    // ---------------- epilogue helpers (warps 7..10): the second half of each
+    // one-accumulator item's steps
+    uint32_t n_done = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n_done) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.acc_full[0], n_done & 1))) {
+        record_error(status, RVQ_DEVICE_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      float4 bq[NCS];
+#pragma unroll
+      for (int k = 0; k < NCS; ++k) bq[k] = bias4(item, k);
+#pragma unroll
+      for (int e = NE / 2; e < NE; ++e) {
+        float v[32];
+        epi_load(0, e, v);
+        tmem_wait_ld();
+        epi_put(item, e, v, bq[e % NCS]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.acc_empty[0]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1284,13 +1314,13 @@ cudaError_t launch_project_tc(const rvq_dims &dm, const void *tables, const floa
   const float *b_in = at<float>(tables, L.b_in);
   const int zs = zero_status ? 1 : 0;
   if (shape == 0)
-    k_project_tc<2, 256><<<grid, PJ_THREADS, pj_smem<2, 256>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+    k_project_tc<2, 256><<<grid, PjShape<2, 256>::THREADS, pj_smem<2, 256>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
                                                                       items, n_cb, status, zs);
   else if (shape == 1)
-    k_project_tc<1, 128><<<grid, PJ_THREADS, pj_smem<1, 128>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+    k_project_tc<1, 128><<<grid, PjShape<1, 128>::THREADS, pj_smem<1, 128>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
                                                                       items, n_cb, status, zs);
   else
-    k_project_tc<1, 64><<<grid, PJ_THREADS, pj_smem<1, 64>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
+    k_project_tc<1, 64><<<grid, PjShape<1, 64>::THREADS, pj_smem<1, 64>(), st>>>(tm_x, tm_whi, tm_wlo, b_in, p0, n, n_cols, D,
                                                                     items, n_cb, status, zs);
   return cudaGetLastError();
 }
