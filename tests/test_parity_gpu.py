@@ -270,6 +270,24 @@ def test_stage_blocks_keep_the_unblocked_sums(K, Q, d, prefixes):
         rq.rvq_set_stream_max_frames(prev)
 
 
+def test_prefix_depths_on_full_width_projection_items():
+    """12 000 frames project as 256-frame x 256-column items, whose epilogue
+    two crews of warps share (the first tile's steps and the second's); prefix
+    depths of 3 and 5 stages leave the last column block part-filled (192 and
+    320 columns): the codes equal the first stages of the full depth, and
+    sampled frames of the full depth match the oracle."""
+    w, W = _small_weights(D=1024, K=1024, Q=8, seed=31, bias=True)
+    x = np.random.default_rng(31).standard_normal((12000, 1024)).astype(np.float32)
+    rvq = make_rvq(W)
+    xt = torch.from_numpy(x).to(DEV)
+    full = rvq.encode(xt).cpu().numpy()
+    for n_q in (3, 5):
+        part = rvq.encode(xt, n_q).cpu().numpy()
+        assert np.array_equal(part, full[:, :n_q]), f"prefix {n_q}"
+    rows = np.concatenate([np.random.default_rng(1).choice(12000, 400, replace=False), [0, 255, 256, 11999]])
+    check_encode(W, x, full, rows=rows, label="full-width items")
+
+
 def test_biases_and_prefix_depths():
     w, W = _small_weights(D=256, K=512, Q=6, bias=True)
     x = np.random.default_rng(5).standard_normal((500, 256)).astype(np.float32)
