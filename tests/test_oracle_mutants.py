@@ -43,6 +43,22 @@ MUTANTS = {
     "fc2_bias_dropped": ("if (fc2_b) t += (double)fc2_b[i];", "if (false) t += (double)fc2_b[i];"),
     "fc2_transposed": ("for (int j = 0; j < D; ++j) t += (double)row[j] * acc[j];",
                        "for (int j = 0; j < D; ++j) t += (double)fc2_w[(size_t)j * D_out + i] * acc[j];"),
+    # a stage index dropped (every stage reads stage 0's weights), the update skipped
+    "encode_w_in_of_stage_zero": ("const float *Win = W.w_in + (size_t)k * d * D;", "const float *Win = W.w_in;"),
+    "encode_b_in_of_stage_zero": ("s += (double)W.b_in[(size_t)k * d + j];", "s += (double)W.b_in[j];"),
+    "encode_b_out_of_stage_zero": ("if (W.b_out) s += (double)W.b_out[(size_t)k * D + i];",
+                                   "if (W.b_out) s += (double)W.b_out[i];"),
+    "residual_not_updated": ("residual[i] -= s;", "(void)s;"),
+    "decode_codebook_of_stage_zero": ("const float *e = codebook + ((size_t)k * K + code) * d;",
+                                      "const float *e = codebook + (size_t)code * d;"),
+    "decode_b_out_of_stage_zero": ("if (b_out) s += (double)b_out[(size_t)k * D + i];",
+                                   "if (b_out) s += (double)b_out[i];"),
+    # bad decode codes: read as row 0 instead of skipped, or skipped without counting
+    "decode_bad_code_read_as_row_zero": ("bad_per_frame[(size_t)n] += 1;\n          continue;",
+                                         "bad_per_frame[(size_t)n] += 1;\n          code = 0;"),
+    "decode_bad_code_not_counted": ("bad_per_frame[(size_t)n] += 1;", "(void)0;"),
+    # the reported best distance is the runner-up's
+    "best_dist_is_second": ("if (best_dist) best_dist[k] = d1;", "if (best_dist) best_dist[k] = d2;"),
 }
 
 PINS = [
